@@ -1,0 +1,33 @@
+"""fp16 GEMM with fp32 accumulation for GB300 (sm_103a).
+
+    C[M,N] = A[M,K] @ B[K,N]   (fp16 in, fp32 accumulate, fp16 out, rounded once)
+
+The work runs in hand-written tcgen05/TMA kernels behind a C ABI
+(include/gemm_sm103.h, libgemm_sm103.so); this package is its thin Python
+binding plus the seeded synthetic inputs used by the tests and the benchmark.
+"""
+from ._binding import (  # noqa: F401
+    DEFAULT_GROUP_SIZE_M,
+    GEMM_ERR_CUDA,
+    GEMM_ERR_INVALID_ARG,
+    GEMM_ERR_TIMEOUT,
+    GEMM_ERR_UNSUPPORTED,
+    GEMM_OK,
+    TILE_128x64x32,
+    TILE_128x256x64,
+    TILE_AUTO,
+    GemmError,
+    gemm,
+    header_functions,
+    last_cuda_error,
+    launch_count,
+    lib_path,
+    load,
+    query_status,
+    set_fault_injection,
+    set_watchdog_ns,
+    status_string,
+    tile_schedule,
+    tile_shape,
+)
+from ._build import build  # noqa: F401

@@ -1,0 +1,198 @@
+"""ctypes binding of libgemm_sm103.so (include/gemm_sm103.h).
+
+Argument marshalling only: tensors are checked and turned into device
+pointers, extents and the current CUDA stream; every step of the GEMM runs in
+the library's kernels. There is no fallback: if the library is missing or the
+tensors are not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import _build
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_UNSUPPORTED = 2
+GEMM_ERR_CUDA = 3
+GEMM_ERR_TIMEOUT = 4
+
+TILE_AUTO = 0
+TILE_128x256x64 = 1
+TILE_128x64x32 = 2
+
+DEFAULT_GROUP_SIZE_M = 8
+
+HEADER = os.path.join(_build.ROOT, "include", "gemm_sm103.h")
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (code {code})")
+
+
+_lib = None
+
+_c_void_p = ctypes.c_void_p
+_SIGNATURES = {
+    "gemm_f16_f32acc": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_int64, ctypes.c_int32, _c_void_p]),
+    "gemm_f16_f32acc_tiled": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _c_void_p,
+                                             _c_void_p]),
+    "gemm_tile_shape": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                       _c_void_p, _c_void_p, _c_void_p]),
+    "gemm_tile_schedule": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_int32, _c_void_p, _c_void_p, _c_void_p]),
+    "gemm_query_status": (ctypes.c_int, [_c_void_p]),
+    "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gemm_last_cuda_error": (ctypes.c_int, []),
+    "gemm_set_watchdog_ns": (ctypes.c_int, [ctypes.c_uint64]),
+    "gemm_set_fault_injection": (ctypes.c_int, [ctypes.c_int32]),
+    "gemm_launch_count": (ctypes.c_uint64, []),
+}
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """The loaded library. Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with dense_fp16_gemm_fp32_gb300.build() (needs nvcc); "
+                "there is no fallback implementation")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/gemm_sm103.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gemm_\w+)\s*\(", text, flags=re.M)
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().gemm_status_string(int(code)).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+def _check(rc: int, what: str):
+    if rc != GEMM_OK:
+        raise GemmError(rc, what)
+
+
+def _stream_ptr(device: torch.device):
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check_operand(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float16:
+        raise TypeError(f"{name} must be float16, got {t.dtype}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device, got {t.device}")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major)")
+
+
+def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZE_M,
+         out: torch.Tensor | None = None, tile_cfg: int = TILE_AUTO,
+         trace: torch.Tensor | None = None) -> torch.Tensor:
+    """C = a @ b with fp16 operands, fp32 accumulation and one fp16 rounding.
+
+    a: [M,K] fp16 CUDA contiguous; b: [K,N] fp16 CUDA contiguous, same device.
+    out: optional [M,N] fp16 CUDA contiguous tensor to write.
+    trace: optional int32 CUDA tensor of 3 * num_tiles entries that receives
+    (pid_m, pid_n, cta) per program id, as the kernel's scheduler ran them.
+    Runs on the current CUDA stream of a's device.
+    """
+    _check_operand(a, "a")
+    _check_operand(b, "b")
+    if a.device != b.device:
+        raise ValueError("a and b must be on the same device")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2:
+        raise ValueError(f"inner extents differ: a is {tuple(a.shape)}, b is {tuple(b.shape)}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=a.device)
+    else:
+        _check_operand(out, "out")
+        if tuple(out.shape) != (M, N) or out.device != a.device:
+            raise ValueError(f"out must be [{M},{N}] on {a.device}")
+    trace_ptr = None
+    if trace is not None:
+        if trace.dtype != torch.int32 or trace.device != a.device or not trace.is_contiguous():
+            raise ValueError("trace must be a contiguous int32 tensor on a's device")
+        trace_ptr = trace.data_ptr()
+    lib = load()
+    with torch.cuda.device(a.device):
+        rc = lib.gemm_f16_f32acc_tiled(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K,
+                                       int(group_size_m), int(tile_cfg), trace_ptr, _stream_ptr(a.device))
+    _check(rc, "gemm_f16_f32acc_tiled")
+    return out
+
+
+def tile_shape(tile_cfg: int = TILE_AUTO, M: int = 0, N: int = 0, K: int = 0) -> tuple[int, int, int]:
+    tm, tn, tk = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(load().gemm_tile_shape(int(tile_cfg), M, N, K, ctypes.byref(tm), ctypes.byref(tn), ctypes.byref(tk)),
+           "gemm_tile_shape")
+    return tm.value, tn.value, tk.value
+
+
+def tile_schedule(M: int, N: int, tile_m: int, tile_n: int, group_size_m: int, device=None):
+    """(pid_m, pid_n) int32 CUDA tensors of the device-side grouped map."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    n = -(-M // tile_m) * -(-N // tile_n) if M > 0 and N > 0 else 0
+    pm = torch.empty(max(n, 1), dtype=torch.int32, device=device)
+    pn = torch.empty(max(n, 1), dtype=torch.int32, device=device)
+    with torch.cuda.device(device):
+        rc = load().gemm_tile_schedule(M, N, tile_m, tile_n, group_size_m, pm.data_ptr(), pn.data_ptr(),
+                                       _stream_ptr(device))
+    _check(rc, "gemm_tile_schedule")
+    return pm[:n], pn[:n]
+
+
+def query_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device status."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        return int(load().gemm_query_status(_stream_ptr(device)))
+
+
+def set_watchdog_ns(ns: int) -> None:
+    _check(load().gemm_set_watchdog_ns(int(ns)), "gemm_set_watchdog_ns")
+
+
+def set_fault_injection(mode: int) -> None:
+    _check(load().gemm_set_fault_injection(int(mode)), "gemm_set_fault_injection")
+
+
+def launch_count() -> int:
+    return int(load().gemm_launch_count())
+
+
+def last_cuda_error() -> int:
+    return int(load().gemm_last_cuda_error())

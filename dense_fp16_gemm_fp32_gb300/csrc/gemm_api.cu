@@ -1,0 +1,339 @@
+// C ABI of the sm_103a fp16 GEMM (declared in include/gemm_sm103.h):
+// argument validation, TMA tensor-map encoding, per-device state and kernel
+// launch. No torch types; plain pointers, extents and a cudaStream_t.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_kernel.cuh"
+#include "gemm_sm103.h"
+
+namespace {
+
+using namespace gemm103;
+
+using Cfg128x256 = TileCfg<128, 256, 64, 4>;
+using Cfg128x64 = TileCfg<128, 64, 32, 6>;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+constexpr int kNumCfgs = 3;
+constexpr int64_t kMaxExtent = int64_t(1) << 30;
+constexpr uint64_t kDefaultWatchdogNs = 2000000000ull;
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    uint32_t* status = nullptr;  // one word, cudaMalloc'd on first use
+    bool attr_set[kNumCfgs] = {};
+    int ctas_per_sm[kNumCfgs] = {};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+std::atomic<int> g_last_cuda_error{0};
+std::atomic<uint64_t> g_watchdog_ns{0};
+std::atomic<int> g_fault_mode{0};
+std::atomic<uint64_t> g_launches{0};
+
+int cuda_fail(cudaError_t e)
+{
+    g_last_cuda_error.store(static_cast<int>(e));
+    return GEMM_ERR_CUDA;
+}
+
+uint64_t watchdog_ns()
+{
+    const uint64_t v = g_watchdog_ns.load();
+    if (v != 0) return v;
+    const char* env = std::getenv("GEMM_WATCHDOG_NS");
+    if (env != nullptr) {
+        const unsigned long long e = std::strtoull(env, nullptr, 10);
+        if (e > 0) return e;
+    }
+    return kDefaultWatchdogNs;
+}
+
+// Per-device state; allocates the status word on the first call.
+int device_state(DeviceState** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (d.status == nullptr) {
+            e = cudaMalloc(&d.status, sizeof(uint32_t));
+            if (e != cudaSuccess) return cuda_fail(e);
+            e = cudaMemset(d.status, 0, sizeof(uint32_t));
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return GEMM_OK;
+}
+
+int encode_fn(EncodeTiledFn* fn)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_encode == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (q != cudaDriverEntryPointSuccess || p == nullptr) return cuda_fail(cudaErrorSymbolNotFound);
+        g_encode = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    *fn = g_encode;
+    return GEMM_OK;
+}
+
+// 2-D fp16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// row pitch `pitch_elems`; box of box_inner x box_outer; zero fill out of bounds.
+int make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
+             uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz)
+{
+    EncodeTiledFn fn = nullptr;
+    int rc = encode_fn(&fn);
+    if (rc != GEMM_OK) return rc;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {pitch_elems * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return GEMM_OK;
+}
+
+struct Problem {
+    const void* A;
+    const void* B;
+    void* C;
+    int64_t M, N, K;
+    int32_t group_size_m;
+};
+
+int validate(const Problem& pr)
+{
+    if (pr.M < 0 || pr.N < 0 || pr.K < 0 || pr.group_size_m <= 0) return GEMM_ERR_INVALID_ARG;
+    if (pr.M > kMaxExtent || pr.N > kMaxExtent || pr.K > kMaxExtent) return GEMM_ERR_UNSUPPORTED;
+    if (pr.M == 0 || pr.N == 0) return GEMM_OK;
+    if (pr.C == nullptr || (pr.K > 0 && (pr.A == nullptr || pr.B == nullptr))) return GEMM_ERR_INVALID_ARG;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(pr.A), b = reinterpret_cast<uintptr_t>(pr.B),
+                    c = reinterpret_cast<uintptr_t>(pr.C);
+    if ((c & 15u) != 0 || (pr.K > 0 && ((a & 15u) != 0 || (b & 15u) != 0))) return GEMM_ERR_UNSUPPORTED;
+    if ((pr.N & 7) != 0 || (pr.K & 7) != 0) return GEMM_ERR_UNSUPPORTED;
+    // C must not overlap A or B
+    const unsigned __int128 c_end = static_cast<unsigned __int128>(c) + static_cast<unsigned __int128>(pr.M) * pr.N * 2;
+    if (pr.K > 0) {
+        const unsigned __int128 a_end = static_cast<unsigned __int128>(a) + static_cast<unsigned __int128>(pr.M) * pr.K * 2;
+        const unsigned __int128 b_end = static_cast<unsigned __int128>(b) + static_cast<unsigned __int128>(pr.K) * pr.N * 2;
+        if (c < a_end && a < c_end) return GEMM_ERR_INVALID_ARG;
+        if (c < b_end && b < c_end) return GEMM_ERR_INVALID_ARG;
+    }
+    return GEMM_OK;
+}
+
+int resolve_cfg(int32_t tile_cfg, int32_t* tm, int32_t* tn, int32_t* tk)
+{
+    switch (tile_cfg) {
+        case GEMM_TILE_AUTO:
+        case GEMM_TILE_128x256x64:
+            *tm = Cfg128x256::TM, *tn = Cfg128x256::TN, *tk = Cfg128x256::TK;
+            return GEMM_TILE_128x256x64;
+        case GEMM_TILE_128x64x32:
+            *tm = Cfg128x64::TM, *tn = Cfg128x64::TN, *tk = Cfg128x64::TK;
+            return GEMM_TILE_128x64x32;
+        default:
+            return -1;
+    }
+}
+
+template <class Cfg>
+int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
+{
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != GEMM_OK) return rc;
+    auto kernel = gemm_f16_f32acc_kernel<Cfg>;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!d->attr_set[cfg_id]) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+            if (e != cudaSuccess) return cuda_fail(e);
+            int occ = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, Cfg::NUM_THREADS, Cfg::SMEM_BYTES);
+            if (e != cudaSuccess) return cuda_fail(e);
+            const int tmem_fit = static_cast<int>(512u / Cfg::TMEM_COLS);
+            d->ctas_per_sm[cfg_id] = occ < 1 ? 1 : (occ < tmem_fit ? occ : tmem_fit);
+            d->attr_set[cfg_id] = true;
+        }
+    }
+
+    const int64_t num_pid_m = (pr.M + Cfg::TM - 1) / Cfg::TM;
+    const int64_t num_pid_n = (pr.N + Cfg::TN - 1) / Cfg::TN;
+    const int64_t num_tiles = num_pid_m * num_pid_n;
+    if (num_tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof(ma));
+    std::memset(&mb, 0, sizeof(mb));
+    if (pr.K > 0) {
+        const CUtensorMapSwizzle a_swz = Cfg::TK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        rc = make_map(&ma, pr.A, pr.K, pr.M, pr.K, Cfg::TK, Cfg::TM, a_swz);
+        if (rc != GEMM_OK) return rc;
+        rc = make_map(&mb, pr.B, pr.N, pr.K, pr.N, 64, Cfg::TK, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != GEMM_OK) return rc;
+    }
+
+    GemmParams p;
+    p.C = static_cast<uint16_t*>(pr.C);
+    p.M = static_cast<int32_t>(pr.M);
+    p.N = static_cast<int32_t>(pr.N);
+    p.K = static_cast<int32_t>(pr.K);
+    p.num_pid_m = static_cast<int32_t>(num_pid_m);
+    p.num_pid_n = static_cast<int32_t>(num_pid_n);
+    p.num_tiles = static_cast<int32_t>(num_tiles);
+    p.num_k_tiles = static_cast<int32_t>((pr.K + Cfg::TK - 1) / Cfg::TK);
+    p.group_size_m = pr.group_size_m > p.num_pid_m ? p.num_pid_m : pr.group_size_m;
+    p.status = d->status;
+    p.trace = trace;
+    p.watchdog_ns = watchdog_ns();
+    p.fault_mode = g_fault_mode.load();
+
+    const int64_t slots = static_cast<int64_t>(d->sm_count) * d->ctas_per_sm[cfg_id];
+    const unsigned grid = static_cast<unsigned>(num_tiles < slots ? num_tiles : slots);
+    kernel<<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(ma, mb, p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                          int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace, void* stream)
+{
+    const Problem pr{A, B, C, M, N, K, group_size_m};
+    int32_t tm, tn, tk;
+    const int cfg = resolve_cfg(tile_cfg, &tm, &tn, &tk);
+    if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
+    int rc = validate(pr);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (cfg) {
+        case GEMM_TILE_128x64x32:
+            return launch<Cfg128x64>(pr, cfg, tile_trace, s);
+        default:
+            return launch<Cfg128x256>(pr, cfg, tile_trace, s);
+    }
+}
+
+int gemm_f16_f32acc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int32_t group_size_m,
+                    void* stream)
+{
+    return gemm_f16_f32acc_tiled(A, B, C, M, N, K, group_size_m, GEMM_TILE_AUTO, nullptr, stream);
+}
+
+int gemm_tile_shape(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tile_m, int32_t* tile_n,
+                    int32_t* tile_k)
+{
+    (void)M, (void)N, (void)K;
+    int32_t tm, tn, tk;
+    if (resolve_cfg(tile_cfg, &tm, &tn, &tk) < 0) return GEMM_ERR_UNSUPPORTED;
+    if (tile_m) *tile_m = tm;
+    if (tile_n) *tile_n = tn;
+    if (tile_k) *tile_k = tk;
+    return GEMM_OK;
+}
+
+int gemm_tile_schedule(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n, int32_t group_size_m, int32_t* d_pid_m,
+                       int32_t* d_pid_n, void* stream)
+{
+    if (M < 0 || N < 0 || tile_m <= 0 || tile_n <= 0 || group_size_m <= 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t num_pid_m = (M + tile_m - 1) / tile_m;
+    const int64_t num_pid_n = (N + tile_n - 1) / tile_n;
+    const int64_t num_tiles = num_pid_m * num_pid_n;
+    if (num_tiles == 0) return GEMM_OK;
+    if (num_tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    if (d_pid_m == nullptr || d_pid_n == nullptr) return GEMM_ERR_INVALID_ARG;
+    const int32_t g = group_size_m > num_pid_m ? static_cast<int32_t>(num_pid_m) : group_size_m;
+    const int threads = 256;
+    const int64_t blocks64 = (num_tiles + threads - 1) / threads;
+    const unsigned blocks = static_cast<unsigned>(blocks64 < 65535 ? blocks64 : 65535);
+    tile_schedule_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<int32_t>(num_tiles), static_cast<int32_t>(num_pid_m), static_cast<int32_t>(num_pid_n), g, d_pid_m,
+        d_pid_n);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
+int gemm_query_status(void* stream)
+{
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != GEMM_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t word = 0;
+    e = cudaMemcpy(&word, d->status, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (word != 0) {
+        e = cudaMemset(d->status, 0, sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return (word & kStatusTimeout) ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+const char* gemm_status_string(int status)
+{
+    switch (status) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid argument";
+        case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: alignment, extent or tile configuration not supported";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: a CUDA runtime call failed";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a kernel's bounded wait expired";
+        default: return "unknown gemm status";
+    }
+}
+
+int gemm_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+int gemm_set_watchdog_ns(uint64_t ns)
+{
+    g_watchdog_ns.store(ns);
+    return GEMM_OK;
+}
+
+int gemm_set_fault_injection(int32_t mode)
+{
+    if (mode < 0 || mode > 1) return GEMM_ERR_INVALID_ARG;
+    g_fault_mode.store(mode);
+    return GEMM_OK;
+}
+
+uint64_t gemm_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,342 @@
+// Persistent, warp-specialised fp16 GEMM with fp32 accumulation for sm_103a.
+//
+//   C[M,N] (fp16) = A[M,K] (fp16, row-major) * B[K,N] (fp16, row-major)
+//
+// The computation is the tiled matrix multiply of "03: Matrix multiplication"
+// (phobos-lang.dev tutorial): a CTA owns a TILE_M x TILE_N tile of C, each turn
+// of the k loop brings a TILE_M x TILE_K panel of A and a TILE_K x TILE_N panel
+// of B into shared memory, their product is added to an fp32 accumulator, and
+// the accumulator is narrowed to fp16 once, when the tile is stored. Tiles are
+// visited in the grouped order of the kernl notebook "2 - matmul offsets.ipynb"
+// (tile_map.cuh).
+//
+// GB300 mapping (one CTA of 192 threads per SM, persistent over tiles):
+//   warp 0, lane 0   TMA producer: per k step, one A box (TILE_K x TILE_M,
+//                    K contiguous) and TILE_N/64 B boxes (64 x TILE_K, N
+//                    contiguous) into an S-stage shared-memory ring, tracked by
+//                    full/empty mbarriers. Loads past M, N or K are zero-filled
+//                    by the TMA unit, so edge tiles need no masking on load and
+//                    a partial last k step adds exact zeros.
+//   warp 1           allocates tensor memory (two TILE_N-column fp32
+//                    accumulators); lane 0 issues tcgen05.mma kind::f16
+//                    (M=128, N=TILE_N, K=16), A K-major and B N-major straight
+//                    from the swizzled shared-memory tiles, and commits each
+//                    stage back to its empty barrier and each finished tile to
+//                    an accumulator-full barrier.
+//   warps 2..5       epilogue: tcgen05.ld of 32 accumulator columns at a time
+//                    (warp w reads TMEM lanes 32*(w%4)..+31, i.e. tile rows),
+//                    one round-to-nearest-even conversion to fp16, and masked
+//                    16-byte stores to C. The accumulator is double buffered,
+//                    so tile i's epilogue runs under tile i+1's main loop.
+// Every mbarrier wait is bounded by %globaltimer; on expiry the CTA records a
+// timeout in the device status word, stops issuing, waits (bounded) for its
+// own copies and MMAs in flight, frees its tensor memory and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+#include "tile_map.cuh"
+
+namespace gemm103 {
+
+// Device status word: bit 0 = a bounded wait expired; bits 8..15 = which role.
+enum : uint32_t { kStatusTimeout = 1u };
+enum : uint32_t { kWhereProducer = 1u, kWhereMma = 2u, kWhereEpilogue = 3u, kWhereDrain = 4u };
+
+struct GemmParams {
+    uint16_t* C;  // fp16 bits, [M,N] row-major
+    int32_t M, N, K;
+    int32_t num_pid_m, num_pid_n, num_tiles, num_k_tiles;
+    int32_t group_size_m;  // already clamped to [1, num_pid_m]
+    uint32_t* status;
+    int32_t* trace;  // NULL or 3 * num_tiles entries
+    uint64_t watchdog_ns;
+    int32_t fault_mode;  // 1: the producer issues nothing (watchdog test)
+};
+
+template <int TM_, int TN_, int TK_, int STAGES_>
+struct TileCfg {
+    static constexpr int TM = TM_, TN = TN_, TK = TK_, STAGES = STAGES_;
+    static_assert(TM == 128, "one-CTA tcgen05 tile: 128 accumulator lanes");
+    static_assert(TN % 64 == 0 && TN >= 64 && TN <= 256, "B is loaded in 64-column boxes; MMA N <= 256");
+    static_assert(TK == 64 || TK == 32, "A rows of 128 B (128B swizzle) or 64 B (64B swizzle)");
+
+    static constexpr int NUM_THREADS = 192;
+    static constexpr int EPI_THREADS = 128;
+
+    static constexpr int A_STAGE = TM * TK * 2;      // bytes of one A panel
+    static constexpr int B_BOX = TK * 64 * 2;        // one 64-column B box: TK rows of 128 B
+    static constexpr int B_STAGE = (TN / 64) * B_BOX;
+    static constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE;
+
+    // A: K-major, rows of TK*2 bytes; core-matrix groups of 8 rows.
+    static constexpr uint32_t A_SWIZZLE = TK == 64 ? kSwizzle128B : kSwizzle64B;
+    static constexpr uint32_t A_SBO = 8 * TK * 2;
+    static constexpr uint32_t A_KSTEP = 32;  // bytes of 16 fp16 along K
+    // B: N-major, rows (one per k) of 64 fp16 = 128 bytes, 128B swizzle;
+    // next 8 k rows at +1024 B, next 64 columns (next box) at +B_BOX.
+    static constexpr uint32_t B_LBO = B_BOX;
+    static constexpr uint32_t B_SBO = 1024;
+    static constexpr uint32_t B_KSTEP = 16 * 128;  // bytes of 16 k rows
+
+    static constexpr uint32_t IDESC = make_idesc_f16_f32acc(TM, TN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+    static constexpr uint32_t TMEM_COLS = (2 * TN <= 32) ? 32 : (2 * TN <= 64) ? 64 : (2 * TN <= 128) ? 128
+                                        : (2 * TN <= 256) ? 256 : 512;
+
+    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 8;
+    static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * (A_STAGE + B_STAGE) + BAR_BYTES;
+    static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+};
+
+struct Watch {
+    volatile uint32_t* abort;  // shared: set by the first wait that expires
+    uint32_t* status;          // global status word
+    uint64_t limit_ns;
+};
+
+// Wait for the phase of `bar` with the given parity. Returns false if the
+// CTA is aborting or the wait exceeded the limit (which starts the abort).
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const Watch& w, uint32_t where)
+{
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(a, parity)) return true;
+        if (*w.abort) return false;
+        if (global_timer_ns() - t0 > w.limit_ns) {
+            *w.abort = 1u;
+            atomicOr(w.status, kStatusTimeout | (where << 8));
+            return false;
+        }
+    }
+}
+
+// Bounded wait used while aborting: ignores the abort flag.
+__device__ __forceinline__ void wait_phase_drain(uint64_t* bar, uint32_t parity, const Watch& w)
+{
+    const uint32_t a = smem_addr(bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, parity)) {
+        if (global_timer_ns() - t0 > w.limit_ns) {
+            atomicOr(w.status, kStatusTimeout | (kWhereDrain << 8));
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_half2_rn(uint32_t lo_bits, uint32_t hi_bits)
+{
+    const __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
+    gemm_f16_f32acc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                           const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // swizzled tiles need 1024 B alignment
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + Cfg::STAGES * Cfg::A_STAGE;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + Cfg::STAGES * Cfg::B_STAGE);
+    uint64_t* empty = full + Cfg::STAGES;
+    uint64_t* acc_full = empty + Cfg::STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], Cfg::EPI_THREADS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+        if (p.num_k_tiles > 0) {
+            tma_prefetch_desc(&tmap_a);
+            tma_prefetch_desc(&tmap_b);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const Watch w{abort_flag, p.status, p.watchdog_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && p.num_k_tiles > 0 && p.fault_mode != 1) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, issued_parity = 0;  // per stage: ever issued / parity of the last issue
+            bool ok = true;
+            for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
+                const int32_t m0 = tc.pid_m * Cfg::TM;
+                const int32_t n0 = tc.pid_n * Cfg::TN;
+                for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
+                    if (!wait_phase(&empty[stage], phase ^ 1u, w, kWhereProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_TX);
+                    const int32_t k0 = kt * Cfg::TK;
+                    tma_load_2d(sA + stage * Cfg::A_STAGE, &tmap_a, &full[stage], k0, m0);
+#pragma unroll
+                    for (int j = 0; j < Cfg::TN / 64; ++j)
+                        tma_load_2d(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmap_b, &full[stage], n0 + 64 * j,
+                                    k0);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == Cfg::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {  // aborting: every load already issued lands before the CTA exits
+                for (int s = 0; s < Cfg::STAGES; ++s)
+                    if (issued & (1u << s)) wait_phase_drain(&full[s], (issued_parity >> s) & 1u, w);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && p.num_k_tiles > 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            const uint32_t a_base = smem_addr(sA);
+            const uint32_t b_base = smem_addr(sB);
+            for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                if (!wait_phase(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::TN);
+                for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
+                    if (!wait_phase(&full[stage], phase, w, kWhereMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_s = a_base + stage * Cfg::A_STAGE;
+                    const uint32_t b_s = b_base + stage * Cfg::B_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < Cfg::TK / 16; ++kk) {
+                        const uint64_t ad = make_smem_desc(a_s + kk * Cfg::A_KSTEP, 16u, Cfg::A_SBO, Cfg::A_SWIZZLE);
+                        const uint64_t bd = make_smem_desc(b_s + kk * Cfg::B_KSTEP, Cfg::B_LBO, Cfg::B_SBO,
+                                                           kSwizzle128B);
+                        tc_mma_f16_ss(d_tmem, ad, bd, Cfg::IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[stage]);  // frees the stage when these MMAs are done
+                    if (++stage == Cfg::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&acc_full[buf]);  // accumulator complete
+                if (++buf == 2) {
+                    buf = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // every MMA issued above has finished before tensor memory is freed
+            tc_commit(drain);
+            wait_phase_drain(drain, 0u, w);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int row = q * 32 + lane;
+        int buf = 0;
+        uint32_t acc_phase = 0;
+        for (int32_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+            const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
+            if (p.trace != nullptr && warp == 2 && lane == 0) {
+                p.trace[3 * static_cast<int64_t>(tile) + 0] = tc.pid_m;
+                p.trace[3 * static_cast<int64_t>(tile) + 1] = tc.pid_n;
+                p.trace[3 * static_cast<int64_t>(tile) + 2] = static_cast<int32_t>(blockIdx.x);
+            }
+            const int32_t gm = tc.pid_m * Cfg::TM + row;
+            const int32_t n0 = tc.pid_n * Cfg::TN;
+            uint16_t* crow = p.C + static_cast<size_t>(gm) * static_cast<size_t>(p.N);
+            if (p.num_k_tiles == 0) {  // K == 0: the empty sum
+                if (gm < p.M) {
+                    for (int32_t c = 0; c < Cfg::TN; c += 8)
+                        if (n0 + c < p.N) *reinterpret_cast<uint4*>(crow + n0 + c) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                continue;
+            }
+            bool ok = wait_phase(&acc_full[buf], acc_phase, w, kWhereEpilogue);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::TN);
+#pragma unroll 1
+            for (int c = 0; c < Cfg::TN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+                tmem_ld_wait();
+                uint32_t h[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r[2 * i], r[2 * i + 1]);
+                if (gm < p.M) {
+                    const int32_t gn = n0 + c * 32;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        if (gn + 8 * v < p.N)
+                            *reinterpret_cast<uint4*>(crow + gn + 8 * v) =
+                                make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&acc_empty[buf]);
+            if (++buf == 2) {
+                buf = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+// The grouped map alone, one thread per pid (same device function as above).
+__global__ void tile_schedule_kernel(int32_t num_tiles, int32_t num_pid_m, int32_t num_pid_n, int32_t group_size_m,
+                                     int32_t* pid_m, int32_t* pid_n)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t pid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; pid < num_tiles; pid += stride) {
+        const TileCoord t = grouped_tile(static_cast<int32_t>(pid), num_pid_m, num_pid_n, group_size_m);
+        pid_m[pid] = t.pid_m;
+        pid_n[pid] = t.pid_n;
+    }
+}
+
+}  // namespace gemm103

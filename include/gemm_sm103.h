@@ -1,0 +1,164 @@
+/*
+ * gemm_sm103.h -- C ABI of the GB300 (sm_103a) fp16 GEMM library
+ * (libgemm_sm103.so).
+ *
+ * The operation (from "03: Matrix multiplication", the phobos-lang.dev tutorial:
+ * its kernel and the paragraph under it):
+ *
+ *     C[M,N] = A[M,K] * B[K,N]
+ *
+ * A, B and C are IEEE binary16 (fp16), dense, row-major and contiguous:
+ * element (i,k) of A is at A + i*K + k, (k,j) of B at B + k*N + j, (i,j) of C
+ * at C + i*N + j. Products are summed in fp32 (tcgen05 tensor-core MMAs with
+ * an fp32 accumulator in tensor memory) and each output is converted to fp16
+ * exactly once, round-to-nearest-even, when it is stored.
+ *
+ * Output tiles are visited in the grouped order of the Triton matmul
+ * tutorial's program-id code, as restated and worked through in the kernl
+ * notebook "2 - matmul offsets.ipynb" (its first markdown cell):
+ *   num_pid_m = ceil(M / TILE_M), num_pid_n = ceil(N / TILE_N)
+ *   num_pid_in_group = group_size_m * num_pid_n
+ *   group_id    = pid / num_pid_in_group
+ *   first_pid_m = group_id * group_size_m
+ *   gsm         = min(num_pid_m - first_pid_m, group_size_m)
+ *   pid_m       = first_pid_m + pid % gsm
+ *   pid_n       = (pid % num_pid_in_group) / gsm
+ * A persistent grid of at most one CTA per SM walks pid = blockIdx.x,
+ * blockIdx.x + gridDim.x, ... so the CTAs resident at any moment work on
+ * neighbouring pids and share A and B panels in L2.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named A, B, C, d_* are DEVICE pointers of the current CUDA
+ *     device (cudaGetDevice). The caller owns them; the library keeps no
+ *     reference after the call returns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Work is
+ *     enqueued asynchronously; no host synchronisation happens unless an entry
+ *     point says so.
+ *   - Return value: a gemm_status_t. Argument errors are detected on the host
+ *     before anything is enqueued. GEMM_ERR_CUDA means a CUDA runtime call
+ *     failed; gemm_last_cuda_error() returns its cudaError_t.
+ *   - The library allocates nothing per call. On the first call on a device
+ *     it allocates one 4-byte device status word (cudaMalloc) and sets kernel
+ *     attributes; make that first call before any CUDA-graph stream capture.
+ *     The status word lives until the process exits.
+ */
+#ifndef GEMM_SM103_H
+#define GEMM_SM103_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1, /* negative extent, group_size_m <= 0, NULL with work to do, aliasing */
+    GEMM_ERR_UNSUPPORTED = 2, /* a TMA constraint: pointer not 16-byte aligned, N or K not a
+                                 multiple of 8, an extent above 2^31-1, an unknown tile config */
+    GEMM_ERR_CUDA = 3,        /* a CUDA runtime call failed (see gemm_last_cuda_error) */
+    GEMM_ERR_TIMEOUT = 4      /* a kernel's bounded wait expired (reported by gemm_query_status) */
+} gemm_status_t;
+
+/* Tile configurations (TILE_M x TILE_N x TILE_K). */
+typedef enum {
+    GEMM_TILE_AUTO = 0,       /* the library picks (currently 128x256x64) */
+    GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */
+    GEMM_TILE_128x64x32 = 2   /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
+                                 BLOCK_SIZE_N 64, BLOCK_SIZE_K 32) */
+} gemm_tile_cfg_t;
+
+/*
+ * C = A * B, fp16 in, fp32 accumulate, fp16 out (see the header comment).
+ *
+ *   A            device, fp16 [M,K] row-major; 16-byte aligned
+ *   B            device, fp16 [K,N] row-major; 16-byte aligned
+ *   C            device, fp16 [M,N] row-major; 16-byte aligned; must not
+ *                overlap A or B. Fully overwritten.
+ *   M, N, K      extents, 0 <= M, N, K <= 2^31-1; N % 8 == 0 and K % 8 == 0
+ *                (row pitches must be multiples of 16 bytes for TMA)
+ *   group_size_m GROUP_SIZE_M of the grouped tile order, >= 1. Values above
+ *                num_pid_m give the same order as num_pid_m.
+ *   stream       cudaStream_t
+ *
+ * Edge cases: M == 0 or N == 0 is a no-op returning GEMM_OK. K == 0 writes
+ * C = +0 (the empty sum). Extents that are not whole tiles are handled by the
+ * kernel: the TMA zero-fills loads past M, N and K, and stores are masked.
+ */
+int gemm_f16_f32acc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                    int32_t group_size_m, void* stream);
+
+/*
+ * As gemm_f16_f32acc, with an explicit tile configuration (gemm_tile_cfg_t)
+ * and an optional tile trace.
+ *
+ *   tile_trace   NULL, or a device int32 array of 3 * num_tiles entries
+ *                (num_tiles = ceil(M/TILE_M) * ceil(N/TILE_N)). When given,
+ *                the kernel's scheduler writes, for every pid it processes,
+ *                tile_trace[3*pid + 0] = pid_m, [3*pid + 1] = pid_n,
+ *                [3*pid + 2] = the CTA (blockIdx.x) that processed it.
+ *                Used to check the kernel's own order against the integer map.
+ */
+int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                          int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace, void* stream);
+
+/*
+ * Tile shape a configuration uses for a problem: writes TILE_M, TILE_N,
+ * TILE_K (host pointers, each may be NULL) and returns GEMM_OK, or
+ * GEMM_ERR_UNSUPPORTED for an unknown tile_cfg. No device work.
+ */
+int gemm_tile_shape(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tile_m,
+                    int32_t* tile_n, int32_t* tile_k);
+
+/*
+ * The grouped pid -> (pid_m, pid_n) map, evaluated on the device by the same
+ * device function the GEMM kernel's scheduler calls, for any tile shape.
+ *
+ *   tile_m, tile_n  tile extents, >= 1
+ *   d_pid_m, d_pid_n device int32 arrays of num_tiles entries each (written)
+ * Returns GEMM_ERR_INVALID_ARG for bad extents or NULL outputs with tiles.
+ */
+int gemm_tile_schedule(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n, int32_t group_size_m,
+                       int32_t* d_pid_m, int32_t* d_pid_n, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns GEMM_ERR_TIMEOUT if a kernel launched since the last query
+ * gave up on a bounded wait (its output is then incomplete), GEMM_OK
+ * otherwise, or GEMM_ERR_CUDA if synchronisation failed.
+ */
+int gemm_query_status(void* stream);
+
+/* Static string naming a gemm_status_t value. Never NULL. */
+const char* gemm_status_string(int status);
+
+/* The cudaError_t of the most recent failed CUDA call in this library
+ * (0 if none). */
+int gemm_last_cuda_error(void);
+
+/*
+ * Upper bound, in nanoseconds of %globaltimer, on every mbarrier wait inside
+ * the kernels. When one expires the kernel records GEMM_ERR_TIMEOUT in the
+ * status word, stops issuing work, waits (again bounded) for its copies and
+ * MMAs in flight, frees its tensor memory and returns. 0 restores the default
+ * (2 s, or the GEMM_WATCHDOG_NS environment variable). Process-wide.
+ */
+int gemm_set_watchdog_ns(uint64_t ns);
+
+/*
+ * Test hook for failure detection. mode 0 = off (default); mode 1 = the TMA
+ * producer issues no loads, so the MMA warp's bounded wait on the first stage
+ * expires and the kernel reports GEMM_ERR_TIMEOUT without touching C beyond
+ * what it had already written. No fault, trap or unbounded wait is involved.
+ * Process-wide.
+ */
+int gemm_set_fault_injection(int32_t mode);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t gemm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_SM103_H */

@@ -16,3 +16,23 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+def pytest_collection_modifyitems(config, items):
+    import torch
+
+    if torch.cuda.is_available():
+        return
+    skip = pytest.mark.skip(reason="no CUDA device")
+    for item in items:
+        if "gpu" in item.keywords:
+            item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def gemm_lib():
+    """The CUDA library, built in-tree if needed (GPU tests only)."""
+    import dense_fp16_gemm_fp32_gb300 as g
+
+    g.build()
+    return g.load()

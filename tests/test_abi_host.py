@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+function include/gemm_sm103.h declares, and argument validation answers
+without a GPU (validation runs before any CUDA call)."""
+import ctypes
+
+import pytest
+import torch
+
+import dense_fp16_gemm_fp32_gb300 as g
+
+
+@pytest.fixture(scope="module")
+def lib():
+    g.build()
+    return g.load()
+
+
+def test_header_declares_expected_entry_points():
+    names = g.header_functions()
+    for want in ("gemm_f16_f32acc", "gemm_f16_f32acc_tiled", "gemm_tile_schedule", "gemm_query_status",
+                 "gemm_status_string", "gemm_tile_shape", "gemm_set_watchdog_ns", "gemm_set_fault_injection",
+                 "gemm_launch_count", "gemm_last_cuda_error"):
+        assert want in names
+    assert len(names) == len(set(names))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(g.lib_path())
+    for name in g.header_functions():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = g.status_string(code)
+        assert s.startswith("GEMM_")
+    assert "unknown" in g.status_string(99)
+
+
+def test_tile_shapes(lib):
+    assert g.tile_shape(g.TILE_AUTO) == (128, 256, 64)
+    assert g.tile_shape(g.TILE_128x256x64) == (128, 256, 64)
+    assert g.tile_shape(g.TILE_128x64x32) == (128, 64, 32)
+    with pytest.raises(g.GemmError) as e:
+        g.tile_shape(17)
+    assert e.value.code == g.GEMM_ERR_UNSUPPORTED
+
+
+def _call(lib, A=16, B=16, C=16, M=64, N=64, K=64, G=8, cfg=0):
+    return lib.gemm_f16_f32acc_tiled(A, B, C, M, N, K, G, cfg, None, None)
+
+
+def test_validation_without_gpu(lib):
+    inv, uns = g.GEMM_ERR_INVALID_ARG, g.GEMM_ERR_UNSUPPORTED
+    big = 1 << 40
+    assert _call(lib, M=-1) == inv
+    assert _call(lib, N=-1) == inv
+    assert _call(lib, K=-1) == inv
+    assert _call(lib, G=0) == inv
+    assert _call(lib, G=-3) == inv
+    assert _call(lib, C=0) == inv                       # NULL C with work to do
+    assert _call(lib, A=0) == inv                       # NULL A with K > 0
+    assert _call(lib, A=24) == uns                      # 8-byte aligned only
+    assert _call(lib, B=big + 2) == uns
+    assert _call(lib, C=big + 8) == uns
+    assert _call(lib, N=60) == uns                      # row pitch not a multiple of 16 B
+    assert _call(lib, K=100) == uns
+    assert _call(lib, M=(1 << 30) + 1) == uns
+    assert _call(lib, cfg=99) == uns
+    # C overlapping A or B
+    assert _call(lib, A=big, B=2 * big, C=big + 4096) == inv
+    assert _call(lib, A=big, B=2 * big, C=2 * big - 16) == inv
+    # no work: OK without touching the device, NULL pointers allowed
+    assert _call(lib, A=0, B=0, C=0, M=0) == g.GEMM_OK
+    assert _call(lib, A=0, B=0, C=0, N=0) == g.GEMM_OK
+    assert lib.gemm_f16_f32acc(0, 0, 0, 0, 5, 5, 1, None) == g.GEMM_OK
+
+
+def test_tile_schedule_validation_without_gpu(lib):
+    assert lib.gemm_tile_schedule(-1, 4, 128, 64, 2, None, None, None) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_tile_schedule(4, 4, 0, 64, 2, None, None, None) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_tile_schedule(4, 4, 128, 64, 0, None, None, None) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_tile_schedule(0, 4, 128, 64, 2, None, None, None) == g.GEMM_OK
+    assert lib.gemm_tile_schedule(4, 4, 128, 64, 2, None, None, None) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_fault_injection_and_watchdog_setters(lib):
+    assert lib.gemm_set_fault_injection(2) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_set_fault_injection(0) == g.GEMM_OK
+    assert lib.gemm_set_watchdog_ns(0) == g.GEMM_OK
+
+
+def test_python_binding_rejects_host_tensors(lib):
+    a = torch.zeros((8, 8), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        g.gemm(a, a)
+    with pytest.raises(TypeError):
+        g.gemm(a.float(), a)

@@ -1,0 +1,130 @@
+"""GPU parity: the CUDA path against the CPU oracle on the same seeded inputs.
+
+Full-size workloads are compared on every row where the oracle is quick
+(M*N*K <= 1.3e10) and on 256 seeded rows otherwise; small and ragged shapes
+cover several tiles plus a partial tile in every dimension.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_fp16_gemm_fp32_gb300 as g
+from dense_fp16_gemm_fp32_gb300 import inputs
+from oracle import gemm as og
+
+from _gpu_util import check_against_oracle, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("w", inputs.WORKLOADS, ids=lambda w: w.name)
+def test_workload_parity(gemm_lib, w):
+    A, B = inputs.gemm_inputs(w.M, w.N, w.K, w.seed)
+    C = g.gemm(A.cuda(), B.cuda(), group_size_m=w.group_size_m, tile_cfg=w.tile_cfg)
+    assert g.query_status() == g.GEMM_OK
+    rows = inputs.sample_rows(w.M, w.seed) if w.sampled else None
+    maxd, n = check_against_oracle(A, B, C, rows)
+    assert n == (256 if w.sampled else w.M) * w.N
+    del C
+    torch.cuda.empty_cache()
+
+
+EDGE_SHAPES = [
+    # (M, N, K): partial tiles in each dimension, single rows/columns of tiles
+    (1, 8, 8), (7, 8, 16), (127, 64, 64), (128, 256, 64), (129, 264, 72), (255, 120, 1000),
+    (300, 520, 136), (513, 72, 24), (64, 1000, 512), (1000, 56, 8), (3, 3000, 40),
+]
+
+
+@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32])
+@pytest.mark.parametrize("M,N,K", EDGE_SHAPES)
+def test_edge_shapes(gemm_lib, M, N, K, cfg):
+    A, B = inputs.gemm_inputs(M, N, K, seed=M * 7 + N * 13 + K)
+    C = g.gemm(A.cuda(), B.cuda(), group_size_m=3, tile_cfg=cfg)
+    assert g.query_status() == g.GEMM_OK
+    check_against_oracle(A, B, C)
+
+
+@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32])
+def test_k_zero_writes_zeros(gemm_lib, cfg):
+    M, N = 200, 264
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    A = torch.empty((M, 0), dtype=torch.float16, device="cuda")
+    B = torch.empty((0, N), dtype=torch.float16, device="cuda")
+    g.gemm(A, B, out=C, tile_cfg=cfg)
+    assert g.query_status() == g.GEMM_OK
+    assert torch.all(C.view(torch.int16) == 0)
+
+
+def test_m_or_n_zero_is_noop(gemm_lib):
+    A = torch.zeros((0, 64), dtype=torch.float16, device="cuda")
+    B = torch.zeros((64, 32), dtype=torch.float16, device="cuda")
+    assert g.gemm(A, B).shape == (0, 32)
+    A = torch.zeros((16, 64), dtype=torch.float16, device="cuda")
+    B = torch.zeros((64, 0), dtype=torch.float16, device="cuda")
+    assert g.gemm(A, B).shape == (16, 0)
+
+
+@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32])
+def test_small_integers_exact(gemm_lib, cfg):
+    # every partial sum is an integer below 2^11: any summation order is exact
+    rng = np.random.default_rng(11)
+    M, N, K = 300, 264, 128
+    A = torch.from_numpy(rng.integers(-4, 5, size=(M, K)).astype(np.float16))
+    B = torch.from_numpy(rng.integers(-4, 5, size=(K, N)).astype(np.float16))
+    C = g.gemm(A.cuda(), B.cuda(), tile_cfg=cfg).cpu()
+    ref = og.gemm_rows(A, B)
+    assert np.array_equal(C.numpy().view(np.uint16), ref.view(np.uint16))
+    assert np.array_equal(C.numpy().astype(np.int64), A.numpy().astype(np.int64) @ B.numpy().astype(np.int64))
+
+
+def test_identity_exact(gemm_lib):
+    rng = np.random.default_rng(12)
+    K = 320
+    B = torch.from_numpy(rng.uniform(-100, 100, size=(K, 200)).astype(np.float16))
+    I = torch.eye(K, dtype=torch.float16)
+    C = g.gemm(I.cuda(), B.cuda()).cpu()
+    assert torch.equal(C.view(torch.int16), B.view(torch.int16))
+
+
+def test_single_narrowing_on_device(gemm_lib):
+    # 1024 + 8 * 0.25 over K = 16 (rest zeros): fp32 accumulation gives 1026,
+    # an fp16 running sum would stay at 1024
+    A = torch.zeros((128, 16), dtype=torch.float16)
+    A[:, 0] = 1024.0
+    A[:, 1:9] = 0.25
+    B = torch.ones((16, 64), dtype=torch.float16)
+    C = g.gemm(A.cuda(), B.cuda()).cpu()
+    assert torch.all(C == 1026.0)
+
+
+@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32])
+def test_group_size_does_not_change_values(gemm_lib, cfg):
+    # the grouped order only changes which CTA computes a tile, not how
+    A, B = inputs.gemm_inputs(700, 1000, 520, seed=21)
+    a, b = A.cuda(), B.cuda()
+    ref = g.gemm(a, b, group_size_m=1, tile_cfg=cfg)
+    for G in (2, 3, 8, 64, 10_000):
+        assert torch.equal(g.gemm(a, b, group_size_m=G, tile_cfg=cfg).view(torch.int16), ref.view(torch.int16))
+    check_against_oracle(A, B, ref)
+
+
+def test_deterministic(gemm_lib):
+    A, B = inputs.gemm_inputs(1024, 1024, 2048, seed=22)
+    a, b = A.cuda(), B.cuda()
+    c1 = g.gemm(a, b)
+    c2 = g.gemm(a, b)
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+
+
+def test_non_default_stream_and_out(gemm_lib):
+    A, B = inputs.gemm_inputs(384, 512, 256, seed=23)
+    a, b = A.cuda(), B.cuda()
+    out = torch.empty((384, 512), dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        r = g.gemm(a, b, out=out)
+    s.synchronize()
+    assert r.data_ptr() == out.data_ptr()
+    check_against_oracle(A, B, out)

@@ -1,0 +1,71 @@
+"""The device-side grouped tile map and the GEMM kernel's own tile order,
+checked bit-exactly against the integer oracle (oracle/tile_map.py)."""
+import pytest
+import torch
+
+import dense_fp16_gemm_fp32_gb300 as g
+from dense_fp16_gemm_fp32_gb300 import inputs
+from oracle import tile_map as tm
+
+from _gpu_util import check_against_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+SCHEDULE_CASES = [
+    # (M, N, tile_m, tile_n, G)
+    (1024, 768, 128, 64, 2),          # the notebook's worked example
+    (8192, 8192, 128, 256, 8),
+    (4095, 3000, 128, 256, 8),
+    (7 * 128, 3 * 64, 128, 64, 2),    # clamped last band
+    (7 * 128, 5 * 64, 128, 64, 4),
+    (16384, 16384, 128, 256, 16),
+    (1, 1, 128, 256, 1),
+    (1000, 37, 16, 8, 3),
+    (5000, 3000, 64, 48, 1000),
+]
+
+
+@pytest.mark.parametrize("M,N,TM,TN,G", SCHEDULE_CASES)
+def test_device_tile_map_bit_exact(gemm_lib, M, N, TM, TN, G):
+    pm, pn = g.tile_schedule(M, N, TM, TN, G)
+    want = tm.tile_order(M, N, TM, TN, G)
+    assert pm.numel() == len(want)
+    got = list(zip(pm.cpu().tolist(), pn.cpu().tolist()))
+    assert got == want
+
+
+def test_worked_example_pid60_on_device(gemm_lib):
+    pm, pn = g.tile_schedule(1024, 768, 128, 64, 2)
+    assert pm.numel() == 96
+    assert (int(pm[60]), int(pn[60])) == (4, 6)
+
+
+def _kernel_trace(M, N, K, G, cfg, seed):
+    tmm, tnn, _ = g.tile_shape(cfg)
+    ntiles = -(-M // tmm) * -(-N // tnn)
+    A, B = inputs.gemm_inputs(M, N, K, seed)
+    trace = torch.full((3 * ntiles,), -1, dtype=torch.int32, device="cuda")
+    C = g.gemm(A.cuda(), B.cuda(), group_size_m=G, tile_cfg=cfg, trace=trace)
+    assert g.query_status() == g.GEMM_OK
+    return A, B, C, trace.view(ntiles, 3).cpu(), tmm, tnn
+
+
+@pytest.mark.parametrize("M,N,K,G,cfg", [
+    (1024, 768, 128, 2, g.TILE_128x64x32),     # the worked example, 96 programs
+    (8192, 8192, 256, 8, g.TILE_128x256x64),   # 2048 tiles: many per CTA
+    (4095, 3000, 64, 5, g.TILE_128x256x64),    # ragged grid, clamped band
+    (896, 192, 64, 2, g.TILE_128x64x32),
+])
+def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
+    A, B, C, tr, TM, TN = _kernel_trace(M, N, K, G, cfg, seed=31)
+    want = tm.tile_order(M, N, TM, TN, G)
+    got = [(int(a), int(b)) for a, b in tr[:, :2].tolist()]
+    assert got == want                      # every pid processed once, with the oracle's tile
+    ctas = tr[:, 2]
+    grid = int(ctas.max()) + 1
+    # persistent schedule: CTA b processes pids b, b + grid, b + 2*grid, ...
+    assert torch.equal(ctas, torch.arange(len(want), dtype=torch.int32) % grid)
+    assert grid <= torch.cuda.get_device_properties(0).multi_processor_count * 4
+    if M * N * K <= 1.3e10:
+        check_against_oracle(A, B, C)
