@@ -68,14 +68,14 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def load_traffic(workload: str, tile: str):
+def load_traffic(workload: str, tile: str, group_size_m: int):
     """DRAM bytes per launch recorded by ncu for this kernel source, or None."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    e = d.get(f"{workload}/{tile}")
+    e = d.get(f"{workload}/{tile}/G{group_size_m}")
     if not e or e.get("kernel_hash") != kernel_source_hash():
         return None
     return float(e["dram_bytes_per_launch"])
@@ -341,7 +341,7 @@ def run_ours(args, w, rank, world, local_rank):
         "config": config_dict(w, args, tile),
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": load_traffic(w.name, tile),
+                     "frac": achieved / peak, "traffic": load_traffic(w.name, tile, args.group_size_m),
                      "peak_source": f"{peak_src} dense bf16 burst (bf16_tflops, MEASURED_PEAKS.json); "
                                     "fp16 and bf16 share the tensor rate",
                      "kernel": f"gemm_f16_f32acc_kernel {tile}", "kernel_ms": kernel_ms,
