@@ -55,6 +55,8 @@ _SIGNATURES = {
     "gemm_set_watchdog_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "gemm_set_fault_injection": (ctypes.c_int, [ctypes.c_int32]),
     "gemm_launch_count": (ctypes.c_uint64, []),
+    "gemm_f16_f32acc_noalloc": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                               ctypes.c_int64, ctypes.c_int32, _c_void_p, _c_void_p]),
 }
 
 

@@ -228,6 +228,66 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
 
 }  // namespace
 
+// ---------------------------------------------------------------- no-alloc variant
+// Scratch for gemm_f16_f32acc_noalloc. Some callers may not allocate device
+// memory at the moment they run a GEMM: code being captured into a CUDA graph
+// (cudaMalloc is refused during capture), plugin hooks of inference runtimes
+// whose enqueue step forbids allocation, or runtimes that hand out all device
+// memory through their own allocator. The default entry point allocates its
+// 4-byte status word with cudaMalloc on its first call on a device; this
+// variant keeps that word in the array below instead, so it never allocates.
+// Word 0 is the status word of the call in flight; the rest is headroom.
+// The array exists on every GPU that loads the library until the process exits.
+constexpr int kNoAllocScratchWords = 64;  // 256 bytes
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
+
+namespace {
+
+struct NoAllocDeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    int ctas_per_sm = 1;
+    uint32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocDeviceState g_noalloc_dev[kMaxDevices];
+
+// Scratch words one call needs: the status word, whatever the extents.
+constexpr int64_t noalloc_scratch_words_needed() { return 1; }
+
+// First call on a device (that device current): resolve the scratch array's
+// device address and set the kernel's shared-memory attribute. Allocates nothing.
+int noalloc_setup(NoAllocDeviceState** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    NoAllocDeviceState& d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        auto kernel = gemm_f16_f32acc_kernel<Cfg128x256>;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg128x256::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e);
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, Cfg128x256::NUM_THREADS,
+                                                          Cfg128x256::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const int tmem_fit = static_cast<int>(512u / Cfg128x256::TMEM_COLS);
+        d.ctas_per_sm = occ < 1 ? 1 : (occ < tmem_fit ? occ : tmem_fit);
+        d.scratch = static_cast<uint32_t*>(ptr);
+        d.ready = true;
+    }
+    *out = &d;
+    return GEMM_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
@@ -335,5 +395,64 @@ int gemm_set_fault_injection(int32_t mode)
 }
 
 uint64_t gemm_launch_count(void) { return g_launches.load(); }
+
+int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                            int32_t group_size_m, uint32_t* d_status, void* stream)
+{
+    const Problem pr{A, B, C, M, N, K, group_size_m};
+    int rc = validate(pr);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    if (noalloc_scratch_words_needed() > kNoAllocScratchWords) return GEMM_ERR_UNSUPPORTED;
+    NoAllocDeviceState* d = nullptr;
+    rc = noalloc_setup(&d);
+    if (rc != GEMM_OK) return rc;
+
+    using Cfg = Cfg128x256;
+    const int64_t num_pid_m = (M + Cfg::TM - 1) / Cfg::TM;
+    const int64_t num_pid_n = (N + Cfg::TN - 1) / Cfg::TN;
+    const int64_t num_tiles = num_pid_m * num_pid_n;
+    if (num_tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof(ma));
+    std::memset(&mb, 0, sizeof(mb));
+    if (K > 0) {
+        rc = make_map(&ma, A, K, M, K, Cfg::TK, Cfg::TM, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != GEMM_OK) return rc;
+        rc = make_map(&mb, B, N, K, N, 64, Cfg::TK, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != GEMM_OK) return rc;
+    }
+
+    GemmParams p;
+    p.C = static_cast<uint16_t*>(C);
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.num_pid_m = static_cast<int32_t>(num_pid_m);
+    p.num_pid_n = static_cast<int32_t>(num_pid_n);
+    p.num_tiles = static_cast<int32_t>(num_tiles);
+    p.num_k_tiles = static_cast<int32_t>((K + Cfg::TK - 1) / Cfg::TK);
+    p.group_size_m = group_size_m > p.num_pid_m ? p.num_pid_m : group_size_m;
+    p.status = d->scratch;  // word 0 of the static scratch array
+    p.trace = nullptr;
+    p.watchdog_ns = watchdog_ns();
+    p.fault_mode = 0;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The scratch keeps the previous call's contents: the status word starts at zero.
+    cudaError_t e = cudaMemsetAsync(d->scratch, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int64_t slots = static_cast<int64_t>(d->sm_count) * d->ctas_per_sm;
+    const unsigned grid = static_cast<unsigned>(num_tiles < slots ? num_tiles : slots);
+    gemm_f16_f32acc_kernel<Cfg><<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1);
+    if (d_status != nullptr) {
+        e = cudaMemcpyAsync(d_status, d->scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return GEMM_OK;
+}
 
 }  // extern "C"

@@ -157,6 +157,38 @@ int gemm_set_fault_injection(int32_t mode);
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t gemm_launch_count(void);
 
+/*
+ * gemm_f16_f32acc_noalloc -- the same GEMM as gemm_f16_f32acc (default tile
+ * configuration), for callers that cannot allocate device memory when they
+ * call it. The pages have no counterpart to this entry point: it exists for
+ * callers such as code being captured into a CUDA graph (cudaMalloc is
+ * refused during capture), inference-runtime plugins whose enqueue step must
+ * not allocate, or hosts whose device memory is owned by their own allocator.
+ * gemm_f16_f32acc allocates its 4-byte status word with cudaMalloc on its
+ * first call on a device; this entry point calls no cudaMalloc, cudaFree or
+ * allocating library routine. Its only scratch is a file-scope device array
+ * of 256 bytes (64 32-bit words, one word used: the watchdog status word),
+ * present on every GPU that loads the library until the process exits.
+ *
+ *   A, B, C, M, N, K, group_size_m, stream
+ *              as for gemm_f16_f32acc, with the same validation and errors
+ *   d_status   NULL, or a device uint32_t that receives, in stream order after
+ *              the kernel, this call's status word: 0 = complete, bit 0 set =
+ *              a bounded wait expired (the output is then incomplete)
+ *
+ * The first call on a device (with that device current) looks up the
+ * scratch array's device address (cudaGetSymbolAddress) and sets the
+ * kernel's shared-memory attribute; make that first call before any stream
+ * capture. A call whose scratch need exceeds the array is rejected with
+ * GEMM_ERR_UNSUPPORTED before anything is enqueued (this kernel needs one
+ * word for any extents). Every call shares the array, which keeps the last
+ * call's contents: each call clears the status word on its stream before the
+ * kernel runs, so calls that overlap on the GPU (different streams, no
+ * ordering between them) race on it.
+ */
+int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                            int32_t group_size_m, uint32_t* d_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
