@@ -55,7 +55,7 @@ typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = 1, /* negative extent, group_size_m <= 0, NULL with work to do, aliasing */
     GEMM_ERR_UNSUPPORTED = 2, /* a TMA constraint: pointer not 16-byte aligned, N or K not a
-                                 multiple of 8, an extent above 2^31-1, an unknown tile config */
+                                 multiple of 8, an extent above 2^30, an unknown tile config */
     GEMM_ERR_CUDA = 3,        /* a CUDA runtime call failed (see gemm_last_cuda_error) */
     GEMM_ERR_TIMEOUT = 4      /* a kernel's bounded wait expired (reported by gemm_query_status) */
 } gemm_status_t;
@@ -75,7 +75,7 @@ typedef enum {
  *   B            device, fp16 [K,N] row-major; 16-byte aligned
  *   C            device, fp16 [M,N] row-major; 16-byte aligned; must not
  *                overlap A or B. Fully overwritten.
- *   M, N, K      extents, 0 <= M, N, K <= 2^31-1; N % 8 == 0 and K % 8 == 0
+ *   M, N, K      extents, 0 <= M, N, K <= 2^30; N % 8 == 0 and K % 8 == 0
  *                (row pitches must be multiples of 16 bytes for TMA)
  *   group_size_m GROUP_SIZE_M of the grouped tile order, >= 1. Values above
  *                num_pid_m give the same order as num_pid_m.
