@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     GEMM_OK,
     TILE_128x64x32,
     TILE_128x256x64,
+    TILE_256x256x64_PAIR,
     TILE_AUTO,
     GemmError,
     gemm,

@@ -24,6 +24,7 @@ GEMM_ERR_TIMEOUT = 4
 TILE_AUTO = 0
 TILE_128x256x64 = 1
 TILE_128x64x32 = 2
+TILE_256x256x64_PAIR = 3
 
 DEFAULT_GROUP_SIZE_M = 8
 

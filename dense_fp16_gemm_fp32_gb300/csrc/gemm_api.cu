@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "gemm_kernel.cuh"
+#include "gemm_kernel_pair.cuh"
 #include "gemm_sm103.h"
 
 namespace {
@@ -19,13 +20,14 @@ using namespace gemm103;
 
 using Cfg128x256 = TileCfg<128, 256, 64, 4>;
 using Cfg128x64 = TileCfg<128, 64, 32, 6>;
+using CfgPair256 = PairCfg<6>;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumCfgs = 3;
+constexpr int kNumCfgs = 4;
 constexpr int64_t kMaxExtent = int64_t(1) << 30;
 constexpr uint64_t kDefaultWatchdogNs = 2000000000ull;
 
@@ -160,6 +162,9 @@ int resolve_cfg(int32_t tile_cfg, int32_t* tm, int32_t* tn, int32_t* tk)
         case GEMM_TILE_128x64x32:
             *tm = Cfg128x64::TM, *tn = Cfg128x64::TN, *tk = Cfg128x64::TK;
             return GEMM_TILE_128x64x32;
+        case GEMM_TILE_256x256x64_PAIR:
+            *tm = CfgPair256::TM, *tn = CfgPair256::TN, *tk = CfgPair256::TK;
+            return GEMM_TILE_256x256x64_PAIR;
         default:
             return -1;
     }
@@ -221,6 +226,84 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     const unsigned grid = static_cast<unsigned>(num_tiles < slots ? num_tiles : slots);
     kernel<<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(ma, mb, p);
     const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
+// Cluster launch of the CTA-pair kernel: one 2-CTA cluster per 256 x 256 tile
+// slot, as many clusters as can be resident at once (persistent).
+template <class Cfg>
+int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
+{
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != GEMM_OK) return rc;
+    auto kernel = gemm_f16_f32acc_pair_kernel<Cfg>;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!d->attr_set[cfg_id]) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+            if (e != cudaSuccess) return cuda_fail(e);
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(static_cast<unsigned>(2 * d->sm_count), 1, 1);
+            q.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
+            q.dynamicSmemBytes = Cfg::SMEM_BYTES;
+            q.attrs = &attr;
+            q.numAttrs = 1;
+            int clusters = 0;
+            e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &q);
+            if (e != cudaSuccess) return cuda_fail(e);
+            d->ctas_per_sm[cfg_id] = clusters < 1 ? 1 : clusters;  // here: resident clusters per device
+            d->attr_set[cfg_id] = true;
+        }
+    }
+
+    const int64_t num_pid_m = (pr.M + Cfg::TM - 1) / Cfg::TM;
+    const int64_t num_pid_n = (pr.N + Cfg::TN - 1) / Cfg::TN;
+    const int64_t num_tiles = num_pid_m * num_pid_n;
+    if (num_tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof(ma));
+    std::memset(&mb, 0, sizeof(mb));
+    if (pr.K > 0) {
+        rc = make_map(&ma, pr.A, pr.K, pr.M, pr.K, Cfg::TK, Cfg::CTA_M, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != GEMM_OK) return rc;
+        rc = make_map(&mb, pr.B, pr.N, pr.K, pr.N, 64, Cfg::TK, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != GEMM_OK) return rc;
+    }
+
+    GemmParams p;
+    p.C = static_cast<uint16_t*>(pr.C);
+    p.M = static_cast<int32_t>(pr.M);
+    p.N = static_cast<int32_t>(pr.N);
+    p.K = static_cast<int32_t>(pr.K);
+    p.num_pid_m = static_cast<int32_t>(num_pid_m);
+    p.num_pid_n = static_cast<int32_t>(num_pid_n);
+    p.num_tiles = static_cast<int32_t>(num_tiles);
+    p.num_k_tiles = static_cast<int32_t>((pr.K + Cfg::TK - 1) / Cfg::TK);
+    p.group_size_m = pr.group_size_m > p.num_pid_m ? p.num_pid_m : pr.group_size_m;
+    p.status = d->status;
+    p.trace = trace;
+    p.watchdog_ns = watchdog_ns();
+    p.fault_mode = g_fault_mode.load();
+
+    const int64_t slots = d->ctas_per_sm[cfg_id];
+    const int64_t pairs = num_tiles < slots ? num_tiles : slots;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    lc.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = stream;
+    lc.attrs = &attr;
+    lc.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, ma, mb, p);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
     return GEMM_OK;
@@ -303,6 +386,8 @@ int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int6
     switch (cfg) {
         case GEMM_TILE_128x64x32:
             return launch<Cfg128x64>(pr, cfg, tile_trace, s);
+        case GEMM_TILE_256x256x64_PAIR:
+            return launch_pair<CfgPair256>(pr, cfg, tile_trace, s);
         default:
             return launch<Cfg128x256>(pr, cfg, tile_trace, s);
     }

@@ -1,0 +1,296 @@
+// CTA-pair variant of the persistent fp16 GEMM (fp32 accumulation) for sm_103a.
+//
+// Same computation and tile order as gemm_kernel.cuh (the tiled matrix
+// multiply of "03: Matrix multiplication", phobos-lang.dev tutorial, with the
+// grouped order of the kernl notebook "2 - matmul offsets.ipynb"), but each
+// 256 x 256 output tile is computed by a cluster of two CTAs on two SMs with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16):
+//
+//   * CTA r of the pair (r = %cluster_ctarank) loads rows [128r, 128r + 128)
+//     of the tile's A panel and columns [128r, 128r + 128) of its B panel into
+//     its own shared memory; the MMA reads A from each CTA's memory for that
+//     CTA's half of the rows and B from both, so each SM stages 32 KiB per
+//     k step for the same 128 x 256 x 64 of work that costs 48 KiB alone.
+//   * Both CTAs' TMA loads complete on the even CTA's full barrier, which the
+//     even CTA arms with the pair's total byte count.
+//   * One thread of the even CTA issues the MMAs and commits each stage to the
+//     empty barriers of both CTAs and each finished accumulator to the
+//     accumulator-full barriers of both CTAs (one commit per barrier, by its
+//     cluster address).
+//   * Each CTA's epilogue reads its 128 rows of the fp32 accumulator from its
+//     own tensor memory, narrows them once to fp16 and stores them; each
+//     epilogue warp then arrives on the even CTA's accumulator-empty barrier.
+//   * Tensor memory (2 x 256 fp32 columns, double buffered) is allocated and
+//     freed by one warp of each CTA together (cta_group::2).
+// Waits are bounded as in gemm_kernel.cuh. Before a CTA may exit, its
+// producer waits until every stage has been released (so no commit still
+// targets it) and the MMA thread waits until both epilogues have released
+// both accumulators; the pair then meets at a cluster barrier.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "kernel_common.cuh"
+#include "ptx.cuh"
+#include "tile_map.cuh"
+
+namespace gemm103 {
+
+template <int STAGES_>
+struct PairCfg {
+    static constexpr int TM = 256, TN = 256, TK = 64, STAGES = STAGES_;  // tile of the pair
+    static constexpr int CTA_M = 128;                                     // A / D rows per CTA
+    static constexpr int CTA_N = 128;                                     // B columns per CTA
+    static constexpr int NUM_THREADS = 192;
+    static constexpr int EPI_WARPS = 4;
+
+    static constexpr int A_STAGE = CTA_M * TK * 2;        // 16 KiB
+    static constexpr int B_BOX = TK * 64 * 2;             // 8 KiB: 64 columns x TK rows
+    static constexpr int B_STAGE = (CTA_N / 64) * B_BOX;  // 16 KiB
+    static constexpr uint32_t PAIR_STAGE_TX = 2u * (A_STAGE + B_STAGE);
+
+    static constexpr uint32_t A_SBO = 1024;       // 8 rows x 128 B
+    static constexpr uint32_t A_KSTEP = 32;       // 16 fp16 along K
+    static constexpr uint32_t B_LBO = B_BOX;      // next 64 columns
+    static constexpr uint32_t B_SBO = 1024;       // next 8 k rows
+    static constexpr uint32_t B_KSTEP = 16 * 128; // 16 k rows
+
+    static constexpr uint32_t IDESC = make_idesc_f16_f32acc(TM, TN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+    static constexpr uint32_t ACC_COLS = TN;      // one accumulator: 128 lanes x 256 fp32 columns per CTA
+    static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
+
+    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 8;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * (A_STAGE + B_STAGE) + BAR_BYTES;
+    static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+    static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
+};
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
+    gemm_f16_f32acc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                const __grid_constant__ CUtensorMap tmap_b, const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + Cfg::STAGES * Cfg::A_STAGE;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + Cfg::STAGES * Cfg::B_STAGE);
+    uint64_t* empty = full + Cfg::STAGES;
+    uint64_t* acc_full = empty + Cfg::STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
+    const int32_t pair = static_cast<int32_t>(blockIdx.x >> 1);
+    const int32_t num_pairs = static_cast<int32_t>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+            mbar_init(&full[s], 1);   // even CTA: one arrive (with the pair's byte count)
+            mbar_init(&empty[s], 1);  // one commit from the MMA thread
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 2 * Cfg::EPI_WARPS);  // even CTA: every epilogue warp of the pair
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+        if (p.num_k_tiles > 0) {
+            tma_prefetch_desc(&tmap_a);
+            tma_prefetch_desc(&tmap_b);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish_alloc_permit_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_arrive();  // both CTAs' barriers exist before either signals the other
+    cluster_wait();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const Watch w{abort_flag, p.status, p.watchdog_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0 && p.num_k_tiles > 0 && p.fault_mode != 1) {
+            const uint32_t full0_even = map_shared_to_rank(smem_addr(&full[0]), 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int32_t tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
+                const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
+                const int32_t m0 = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M;
+                const int32_t n0 = tc.pid_n * Cfg::TN + static_cast<int32_t>(rank) * Cfg::CTA_N;
+                for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
+                    if (!wait_phase<true>(&empty[stage], phase ^ 1u, w, kWhereProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], Cfg::PAIR_STAGE_TX);
+                    const uint32_t fb = full0_even + 8u * static_cast<uint32_t>(stage);
+                    const int32_t k0 = kt * Cfg::TK;
+                    tma_load_2d_pair(sA + stage * Cfg::A_STAGE, &tmap_a, fb, k0, m0);
+#pragma unroll
+                    for (int j = 0; j < Cfg::CTA_N / 64; ++j)
+                        tma_load_2d_pair(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmap_b, fb, n0 + 64 * j, k0);
+                    if (++stage == Cfg::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every stage released: no commit from the MMA thread still targets this CTA
+            for (int i = 0; ok && i < Cfg::STAGES; ++i) {
+                ok = wait_phase<true>(&empty[stage], phase ^ 1u, w, kWhereProducer);
+                if (++stage == Cfg::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        if (rank == 0 && lane == 0 && p.num_k_tiles > 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            const uint32_t a_base = smem_addr(sA);
+            const uint32_t b_base = smem_addr(sB);
+            const uint32_t empty0_even = map_shared_to_rank(smem_addr(&empty[0]), 0);
+            const uint32_t empty0_odd = map_shared_to_rank(smem_addr(&empty[0]), 1);
+            const uint32_t accf0_even = map_shared_to_rank(smem_addr(&acc_full[0]), 0);
+            const uint32_t accf0_odd = map_shared_to_rank(smem_addr(&acc_full[0]), 1);
+            for (int32_t tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
+                if (!wait_phase<true>(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * Cfg::ACC_COLS;
+                for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
+                    if (!wait_phase(&full[stage], phase, w, kWhereMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_s = a_base + stage * Cfg::A_STAGE;
+                    const uint32_t b_s = b_base + stage * Cfg::B_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < Cfg::TK / 16; ++kk) {
+                        const uint64_t ad = make_smem_desc(a_s + kk * Cfg::A_KSTEP, 16u, Cfg::A_SBO, kSwizzle128B);
+                        const uint64_t bd =
+                            make_smem_desc(b_s + kk * Cfg::B_KSTEP, Cfg::B_LBO, Cfg::B_SBO, kSwizzle128B);
+                        tc_mma_f16_ss_pair(d_tmem, ad, bd, Cfg::IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    const uint32_t off = 8u * static_cast<uint32_t>(stage);
+                    tc_commit_pair(empty0_even + off);  // the stage is free in both CTAs
+                    tc_commit_pair(empty0_odd + off);
+                    if (++stage == Cfg::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair(accf0_even + 8u * static_cast<uint32_t>(buf));  // accumulator complete
+                tc_commit_pair(accf0_odd + 8u * static_cast<uint32_t>(buf));
+                if (++buf == 2) {
+                    buf = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // both epilogues have released both accumulators: no arrive still targets this CTA
+            for (int i = 0; ok && i < 2; ++i) {
+                ok = wait_phase<true>(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma);
+                if (++buf == 2) {
+                    buf = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // every MMA issued above has finished before tensor memory is freed
+            tc_commit_pair(map_shared_to_rank(smem_addr(drain), 0));
+            wait_phase_drain(drain, 0u, w);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t acc_empty0_even = map_shared_to_rank(smem_addr(&acc_empty[0]), 0);
+        int buf = 0;
+        uint32_t acc_phase = 0;
+        for (int32_t tile = pair; tile < p.num_tiles; tile += num_pairs) {
+            const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
+            if (p.trace != nullptr && rank == 0 && warp == 2 && lane == 0) {
+                p.trace[3 * static_cast<int64_t>(tile) + 0] = tc.pid_m;
+                p.trace[3 * static_cast<int64_t>(tile) + 1] = tc.pid_n;
+                p.trace[3 * static_cast<int64_t>(tile) + 2] = pair;
+            }
+            const int32_t gm = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + row;
+            const int32_t n0 = tc.pid_n * Cfg::TN;
+            uint16_t* crow = p.C + static_cast<size_t>(gm) * static_cast<size_t>(p.N);
+            if (p.num_k_tiles == 0) {  // K == 0: the empty sum
+                if (gm < p.M) {
+                    for (int32_t c = 0; c < Cfg::TN; c += 8)
+                        if (n0 + c < p.N) *reinterpret_cast<uint4*>(crow + n0 + c) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                continue;
+            }
+            bool ok = wait_phase<true>(&acc_full[buf], acc_phase, w, kWhereEpilogue);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t t_row =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf) * Cfg::ACC_COLS;
+#pragma unroll 1
+            for (int c = 0; c < Cfg::TN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+                tmem_ld_wait();
+                uint32_t h[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r[2 * i], r[2 * i + 1]);
+                if (gm < p.M) {
+                    const int32_t gn = n0 + c * 32;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        if (gn + 8 * v < p.N)
+                            *reinterpret_cast<uint4*>(crow + gn + 8 * v) =
+                                make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty0_even + 8u * static_cast<uint32_t>(buf));
+            if (++buf == 2) {
+                buf = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort_flag != 0u) {
+        // aborting: give copies already issued by either CTA time to land
+        for (int i = 0; i < 64; ++i) __nanosleep(1000);
+    }
+    cluster_arrive();
+    cluster_wait();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace gemm103

@@ -64,8 +64,10 @@ typedef enum {
 typedef enum {
     GEMM_TILE_AUTO = 0,       /* the library picks (currently 128x256x64) */
     GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */
-    GEMM_TILE_128x64x32 = 2   /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
+    GEMM_TILE_128x64x32 = 2,  /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
                                  BLOCK_SIZE_N 64, BLOCK_SIZE_K 32) */
+    GEMM_TILE_256x256x64_PAIR = 3 /* a 2-CTA cluster per tile (tcgen05 cta_group::2): each
+                                 CTA stages 128 rows of A and 128 columns of B, 6 stages */
 } gemm_tile_cfg_t;
 
 /*
@@ -96,7 +98,8 @@ int gemm_f16_f32acc(const void* A, const void* B, void* C, int64_t M, int64_t N,
  *                (num_tiles = ceil(M/TILE_M) * ceil(N/TILE_N)). When given,
  *                the kernel's scheduler writes, for every pid it processes,
  *                tile_trace[3*pid + 0] = pid_m, [3*pid + 1] = pid_n,
- *                [3*pid + 2] = the CTA (blockIdx.x) that processed it.
+ *                [3*pid + 2] = the CTA (blockIdx.x) that processed it, or for
+ *                GEMM_TILE_256x256x64_PAIR the cluster (blockIdx.x / 2).
  *                Used to check the kernel's own order against the integer map.
  */
 int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,

@@ -12,9 +12,11 @@ import dense_fp16_gemm_fp32_gb300 as g
 from dense_fp16_gemm_fp32_gb300 import inputs
 from oracle import gemm as og
 
-from _gpu_util import check_against_oracle, compare
+from _gpu_util import check_against_oracle
 
 pytestmark = pytest.mark.gpu
+
+ALL_CFGS = [g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x64_PAIR]
 
 
 @pytest.mark.parametrize("w", inputs.WORKLOADS, ids=lambda w: w.name)
@@ -29,14 +31,27 @@ def test_workload_parity(gemm_lib, w):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("w", [w for w in inputs.WORKLOADS if w.tile_cfg == 0], ids=lambda w: w.name)
+@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_256x256x64_PAIR])
+def test_workload_parity_each_large_tile(gemm_lib, w, cfg):
+    A, B = inputs.gemm_inputs(w.M, w.N, w.K, w.seed)
+    C = g.gemm(A.cuda(), B.cuda(), group_size_m=w.group_size_m, tile_cfg=cfg)
+    assert g.query_status() == g.GEMM_OK
+    rows = inputs.sample_rows(w.M, w.seed) if w.sampled else None
+    check_against_oracle(A, B, C, rows)
+    del C
+    torch.cuda.empty_cache()
+
+
 EDGE_SHAPES = [
     # (M, N, K): partial tiles in each dimension, single rows/columns of tiles
     (1, 8, 8), (7, 8, 16), (127, 64, 64), (128, 256, 64), (129, 264, 72), (255, 120, 1000),
     (300, 520, 136), (513, 72, 24), (64, 1000, 512), (1000, 56, 8), (3, 3000, 40),
+    (256, 256, 64), (257, 264, 128), (129, 8, 64), (600, 600, 8),
 ]
 
 
-@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32])
+@pytest.mark.parametrize("cfg", ALL_CFGS)
 @pytest.mark.parametrize("M,N,K", EDGE_SHAPES)
 def test_edge_shapes(gemm_lib, M, N, K, cfg):
     A, B = inputs.gemm_inputs(M, N, K, seed=M * 7 + N * 13 + K)
@@ -45,7 +60,7 @@ def test_edge_shapes(gemm_lib, M, N, K, cfg):
     check_against_oracle(A, B, C)
 
 
-@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32])
+@pytest.mark.parametrize("cfg", ALL_CFGS)
 def test_k_zero_writes_zeros(gemm_lib, cfg):
     M, N = 200, 264
     C = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
@@ -65,7 +80,7 @@ def test_m_or_n_zero_is_noop(gemm_lib):
     assert g.gemm(A, B).shape == (16, 0)
 
 
-@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32])
+@pytest.mark.parametrize("cfg", ALL_CFGS)
 def test_small_integers_exact(gemm_lib, cfg):
     # every partial sum is an integer below 2^11: any summation order is exact
     rng = np.random.default_rng(11)
@@ -98,7 +113,7 @@ def test_single_narrowing_on_device(gemm_lib):
     assert torch.all(C == 1026.0)
 
 
-@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32])
+@pytest.mark.parametrize("cfg", ALL_CFGS)
 def test_group_size_does_not_change_values(gemm_lib, cfg):
     # the grouped order only changes which CTA computes a tile, not how
     A, B = inputs.gemm_inputs(700, 1000, 520, seed=21)
