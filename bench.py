@@ -246,8 +246,9 @@ def run_ours(args, w, rank, world, local_rank):
     A, B = inputs.gemm_inputs(w.M, w.N, w.K, w.seed)
     a, b = A.to(dev), B.to(dev)
     c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
-    tm, tn, tk = g.tile_shape(args.tile_cfg)
-    tile = f"{tm}x{tn}x{tk}"
+    tm, tn, tk = g.tile_shape(args.tile_cfg, w.M, w.N, w.K)
+    tile = f"{tm}x{tn}x{tk}" + ("_pair" if tm == 256 else "")
+    kernel_name = "gemm_f16_f32acc_pair_kernel" if tm == 256 else "gemm_f16_f32acc_kernel"
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
 
@@ -344,7 +345,7 @@ def run_ours(args, w, rank, world, local_rank):
                      "frac": achieved / peak, "traffic": load_traffic(w.name, tile, args.group_size_m),
                      "peak_source": f"{peak_src} dense bf16 burst (bf16_tflops, MEASURED_PEAKS.json); "
                                     "fp16 and bf16 share the tensor rate",
-                     "kernel": f"gemm_f16_f32acc_kernel {tile}", "kernel_ms": kernel_ms,
+                     "kernel": f"{kernel_name} {tile}", "kernel_ms": kernel_ms,
                      "flops_per_launch": flops},
         "e2e": {"value": flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": 2 * (w.M * w.K + w.K * w.N), "d2h_bytes_per_step": 2 * w.M * w.N,
@@ -366,7 +367,7 @@ def main():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="square8192")
-    p.add_argument("--group-size-m", type=int, default=8)
+    p.add_argument("--group-size-m", type=int, default=16)
     p.add_argument("--tile-cfg", type=int, default=0)
     p.add_argument("--flush-l2", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=50)

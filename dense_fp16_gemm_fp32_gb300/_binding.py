@@ -26,7 +26,7 @@ TILE_128x256x64 = 1
 TILE_128x64x32 = 2
 TILE_256x256x64_PAIR = 3
 
-DEFAULT_GROUP_SIZE_M = 8
+DEFAULT_GROUP_SIZE_M = 16
 
 HEADER = os.path.join(_build.ROOT, "include", "gemm_sm103.h")
 

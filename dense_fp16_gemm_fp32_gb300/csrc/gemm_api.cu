@@ -152,10 +152,12 @@ int validate(const Problem& pr)
     return GEMM_OK;
 }
 
-int resolve_cfg(int32_t tile_cfg, int32_t* tm, int32_t* tn, int32_t* tk)
+// GEMM_TILE_AUTO: the CTA-pair 256x256 tile unless the problem has at most
+// one 128-row band, where half of every pair tile would be empty.
+int resolve_cfg(int32_t tile_cfg, int64_t M, int32_t* tm, int32_t* tn, int32_t* tk)
 {
+    if (tile_cfg == GEMM_TILE_AUTO) tile_cfg = M > 128 ? GEMM_TILE_256x256x64_PAIR : GEMM_TILE_128x256x64;
     switch (tile_cfg) {
-        case GEMM_TILE_AUTO:
         case GEMM_TILE_128x256x64:
             *tm = Cfg128x256::TM, *tn = Cfg128x256::TN, *tk = Cfg128x256::TK;
             return GEMM_TILE_128x256x64;
@@ -196,9 +198,12 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     const int64_t num_tiles = num_pid_m * num_pid_n;
     if (num_tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
 
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
+    // C: 32 x 32 store boxes, 64-byte swizzle (matches the epilogue staging layout)
+    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.N, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (rc != GEMM_OK) return rc;
     if (pr.K > 0) {
         const CUtensorMapSwizzle a_swz = Cfg::TK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
         rc = make_map(&ma, pr.A, pr.K, pr.M, pr.K, Cfg::TK, Cfg::TM, a_swz);
@@ -224,7 +229,7 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
 
     const int64_t slots = static_cast<int64_t>(d->sm_count) * d->ctas_per_sm[cfg_id];
     const unsigned grid = static_cast<unsigned>(num_tiles < slots ? num_tiles : slots);
-    kernel<<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(ma, mb, p);
+    kernel<<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(ma, mb, mc, p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
@@ -269,9 +274,12 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     const int64_t num_tiles = num_pid_m * num_pid_n;
     if (num_tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
 
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
+    // C: 32 x 32 store boxes, 64-byte swizzle (matches the epilogue staging layout)
+    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.N, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (rc != GEMM_OK) return rc;
     if (pr.K > 0) {
         rc = make_map(&ma, pr.A, pr.K, pr.M, pr.K, Cfg::TK, Cfg::CTA_M, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != GEMM_OK) return rc;
@@ -303,7 +311,7 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     lc.stream = stream;
     lc.attrs = &attr;
     lc.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, ma, mb, p);
+    const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, ma, mb, mc, p);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
     return GEMM_OK;
@@ -378,7 +386,7 @@ int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int6
 {
     const Problem pr{A, B, C, M, N, K, group_size_m};
     int32_t tm, tn, tk;
-    const int cfg = resolve_cfg(tile_cfg, &tm, &tn, &tk);
+    const int cfg = resolve_cfg(tile_cfg, M, &tm, &tn, &tk);
     if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
     int rc = validate(pr);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
@@ -402,9 +410,9 @@ int gemm_f16_f32acc(const void* A, const void* B, void* C, int64_t M, int64_t N,
 int gemm_tile_shape(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tile_m, int32_t* tile_n,
                     int32_t* tile_k)
 {
-    (void)M, (void)N, (void)K;
+    (void)N, (void)K;
     int32_t tm, tn, tk;
-    if (resolve_cfg(tile_cfg, &tm, &tn, &tk) < 0) return GEMM_ERR_UNSUPPORTED;
+    if (resolve_cfg(tile_cfg, M, &tm, &tn, &tk) < 0) return GEMM_ERR_UNSUPPORTED;
     if (tile_m) *tile_m = tm;
     if (tile_n) *tile_n = tn;
     if (tile_k) *tile_k = tk;
@@ -498,9 +506,11 @@ int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, in
     const int64_t num_tiles = num_pid_m * num_pid_n;
     if (num_tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
 
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
+    rc = make_map(&mc, C, N, M, N, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (rc != GEMM_OK) return rc;
     if (K > 0) {
         rc = make_map(&ma, A, K, M, K, Cfg::TK, Cfg::TM, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != GEMM_OK) return rc;
@@ -529,7 +539,7 @@ int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, in
     if (e != cudaSuccess) return cuda_fail(e);
     const int64_t slots = static_cast<int64_t>(d->sm_count) * d->ctas_per_sm;
     const unsigned grid = static_cast<unsigned>(num_tiles < slots ? num_tiles : slots);
-    gemm_f16_f32acc_kernel<Cfg><<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, p);
+    gemm_f16_f32acc_kernel<Cfg><<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, mc, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);

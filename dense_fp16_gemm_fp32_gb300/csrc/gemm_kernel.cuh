@@ -25,9 +25,11 @@
 //                    an accumulator-full barrier.
 //   warps 2..5       epilogue: tcgen05.ld of 32 accumulator columns at a time
 //                    (warp w reads TMEM lanes 32*(w%4)..+31, i.e. tile rows),
-//                    one round-to-nearest-even conversion to fp16, and masked
-//                    16-byte stores to C. The accumulator is double buffered,
-//                    so tile i's epilogue runs under tile i+1's main loop.
+//                    one round-to-nearest-even conversion to fp16, a swizzled
+//                    shared-memory staging buffer and a TMA store of each
+//                    32 x 32 block (the TMA unit clips rows and columns past C).
+//                    The accumulator is double buffered, so tile i's epilogue
+//                    runs under tile i+1's main loop.
 // Every mbarrier wait is bounded by %globaltimer; on expiry the CTA records a
 // timeout in the device status word, stops issuing, waits (bounded) for its
 // own copies and MMAs in flight, frees its tensor memory and returns.
@@ -72,22 +74,26 @@ struct TileCfg {
     static constexpr uint32_t TMEM_COLS = (2 * TN <= 32) ? 32 : (2 * TN <= 64) ? 64 : (2 * TN <= 128) ? 128
                                         : (2 * TN <= 256) ? 256 : 512;
 
+    static constexpr int EPI_WARPS = EPI_THREADS / 32;
+    static constexpr int STAGING_BYTES = EPI_WARPS * kEpiWarpStagingBytes;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 8;
-    static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * (A_STAGE + B_STAGE) + BAR_BYTES;
+    static constexpr int SMEM_BYTES =
+        1024 /*alignment slack*/ + STAGES * (A_STAGE + B_STAGE) + STAGING_BYTES + BAR_BYTES;
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 };
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     gemm_f16_f32acc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                           const GemmParams p)
+                           const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // swizzled tiles need 1024 B alignment
     uint8_t* sA = smem;
     uint8_t* sB = sA + Cfg::STAGES * Cfg::A_STAGE;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + Cfg::STAGES * Cfg::B_STAGE);
+    uint8_t* sC = sB + Cfg::STAGES * Cfg::B_STAGE;  // epilogue staging, kEpiWarpStagingBytes per warp
+    uint64_t* full = reinterpret_cast<uint64_t*>(sC + Cfg::STAGING_BYTES);
     uint64_t* empty = full + Cfg::STAGES;
     uint64_t* acc_full = empty + Cfg::STAGES;
     uint64_t* acc_empty = acc_full + 2;
@@ -105,7 +111,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], Cfg::EPI_THREADS);
+            mbar_init(&acc_empty[b], Cfg::EPI_WARPS);  // one arrive per epilogue warp
         }
         mbar_init(drain, 1);
         *abort_flag = 0u;
@@ -113,6 +119,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (p.num_k_tiles > 0) {
             tma_prefetch_desc(&tmap_a);
             tma_prefetch_desc(&tmap_b);
+            tma_prefetch_desc(&tmap_c);
         }
     }
     if (warp == 1) {
@@ -236,30 +243,20 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             if (!ok) break;
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::TN);
-#pragma unroll 1
-            for (int c = 0; c < Cfg::TN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
-                tmem_ld_wait();
-                uint32_t h[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r[2 * i], r[2 * i + 1]);
-                if (gm < p.M) {
-                    const int32_t gn = n0 + c * 32;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        if (gn + 8 * v < p.N)
-                            *reinterpret_cast<uint4*>(crow + gn + 8 * v) =
-                                make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
-                }
-            }
-            tc_fence_before_sync();
-            mbar_arrive(&acc_empty[buf]);
+            uint64_t* release_bar = &acc_empty[buf];
+            epilogue_tma_store<Cfg::TN>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c,
+                                        tc.pid_m * Cfg::TM + q * 32, n0, p.M, p.N, lane, [&]() {
+                                            tc_fence_before_sync();
+                                            __syncwarp();
+                                            if (lane == 0) mbar_arrive(release_bar);
+                                        });
             if (++buf == 2) {
                 buf = 0;
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) bulk_wait_group<0>();  // every store of C has completed
+        __syncwarp();
     }
 
     tc_fence_before_sync();

@@ -18,8 +18,9 @@
 //     accumulator-full barriers of both CTAs (one commit per barrier, by its
 //     cluster address).
 //   * Each CTA's epilogue reads its 128 rows of the fp32 accumulator from its
-//     own tensor memory, narrows them once to fp16 and stores them; each
-//     epilogue warp then arrives on the even CTA's accumulator-empty barrier.
+//     own tensor memory, narrows them once to fp16 and writes them with TMA
+//     stores through swizzled staging buffers; each epilogue warp arrives on
+//     the even CTA's accumulator-empty barrier as soon as its reads are done.
 //   * Tensor memory (2 x 256 fp32 columns, double buffered) is allocated and
 //     freed by one warp of each CTA together (cta_group::2).
 // Waits are bounded as in gemm_kernel.cuh. Before a CTA may exit, its
@@ -60,8 +61,9 @@ struct PairCfg {
     static constexpr uint32_t ACC_COLS = TN;      // one accumulator: 128 lanes x 256 fp32 columns per CTA
     static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 
+    static constexpr int STAGING_BYTES = EPI_WARPS * kEpiWarpStagingBytes;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 8;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * (A_STAGE + B_STAGE) + BAR_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * (A_STAGE + B_STAGE) + STAGING_BYTES + BAR_BYTES;
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
     static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
 };
@@ -69,14 +71,16 @@ struct PairCfg {
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     gemm_f16_f32acc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                                const __grid_constant__ CUtensorMap tmap_b, const GemmParams p)
+                                const __grid_constant__ CUtensorMap tmap_b,
+                                const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* sA = smem;
     uint8_t* sB = sA + Cfg::STAGES * Cfg::A_STAGE;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + Cfg::STAGES * Cfg::B_STAGE);
+    uint8_t* sC = sB + Cfg::STAGES * Cfg::B_STAGE;  // epilogue staging, kEpiWarpStagingBytes per warp
+    uint64_t* full = reinterpret_cast<uint64_t*>(sC + Cfg::STAGING_BYTES);
     uint64_t* empty = full + Cfg::STAGES;
     uint64_t* acc_full = empty + Cfg::STAGES;
     uint64_t* acc_empty = acc_full + 2;
@@ -105,6 +109,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         if (p.num_k_tiles > 0) {
             tma_prefetch_desc(&tmap_a);
             tma_prefetch_desc(&tmap_b);
+            tma_prefetch_desc(&tmap_c);
         }
     }
     if (warp == 1) {
@@ -252,31 +257,21 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             tc_fence_after_sync();
             const uint32_t t_row =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf) * Cfg::ACC_COLS;
-#pragma unroll 1
-            for (int c = 0; c < Cfg::TN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
-                tmem_ld_wait();
-                uint32_t h[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r[2 * i], r[2 * i + 1]);
-                if (gm < p.M) {
-                    const int32_t gn = n0 + c * 32;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        if (gn + 8 * v < p.N)
-                            *reinterpret_cast<uint4*>(crow + gn + 8 * v) =
-                                make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
-                }
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty0_even + 8u * static_cast<uint32_t>(buf));
+            const uint32_t release_addr = acc_empty0_even + 8u * static_cast<uint32_t>(buf);
+            epilogue_tma_store<Cfg::TN>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c,
+                                        tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + q * 32, n0,
+                                        p.M, p.N, lane, [&]() {
+                                            tc_fence_before_sync();
+                                            __syncwarp();
+                                            if (lane == 0) mbar_arrive_cluster(release_addr);
+                                        });
             if (++buf == 2) {
                 buf = 0;
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) bulk_wait_group<0>();  // every store of C has completed
+        __syncwarp();
     }
 
     tc_fence_before_sync();

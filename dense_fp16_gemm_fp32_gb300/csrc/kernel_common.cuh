@@ -7,6 +7,8 @@
 
 #include "ptx.cuh"
 
+#include <cuda.h>
+
 namespace gemm103 {
 
 // Device status word: bit 0 = a bounded wait expired; bits 8..15 = which role.
@@ -74,6 +76,58 @@ __device__ __forceinline__ uint32_t pack_half2_rn(uint32_t lo_bits, uint32_t hi_
 {
     const __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
     return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Epilogue staging: each epilogue warp owns two 32-row x 32-column fp16
+// buffers (2 KiB each) laid out with the TMA 64-byte swizzle (16-byte chunk j
+// of row r sits at chunk j ^ ((r >> 1) & 3)), so the 32 lanes' 16-byte
+// shared stores are conflict free and the TMA store reads them unswizzled.
+constexpr int kEpiChunkCols = 32;
+constexpr int kEpiBufBytes = 32 * kEpiChunkCols * 2;
+constexpr int kEpiWarpStagingBytes = 2 * kEpiBufBytes;
+
+// Drains one fp32 accumulator held in tensor memory to C through TMA stores.
+//   t_row     tensor-memory address of (this warp's first lane, first column)
+//   staging   this warp's 2 x 2 KiB staging buffers (1024-byte aligned)
+//   c_row0    first C row of this warp's 32 rows; n0 first C column of the tile
+//   M, N      extents of C
+//   release   called by every lane once all tensor-memory reads are done
+// The accumulator is narrowed to fp16 once (round to nearest even). Parts of
+// a 32 x 32 block outside C are clipped by the TMA unit; blocks entirely
+// outside C are not stored. Only lane 0 issues stores, so lane 0 alone waits
+// on the bulk groups.
+template <int TN, class Release>
+__device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* staging, const CUtensorMap* tmap_c,
+                                                   int32_t c_row0, int32_t n0, int32_t M, int32_t N, int lane,
+                                                   Release release)
+{
+    const uint32_t stage0 = smem_addr(staging);
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 64u;
+    const uint32_t swz = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll 1
+    for (int c = 0; c < TN / kEpiChunkCols; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * kEpiChunkCols), r);
+        tmem_ld_wait();
+        if (c == TN / kEpiChunkCols - 1) release();
+        uint32_t h[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r[2 * i], r[2 * i + 1]);
+        const uint32_t buf = stage0 + static_cast<uint32_t>((c & 1) * kEpiBufBytes);
+        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            st_shared_v4(buf + row_off + ((static_cast<uint32_t>(j) ^ swz) << 4), h[4 * j], h[4 * j + 1], h[4 * j + 2],
+                         h[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            const int32_t x = n0 + c * kEpiChunkCols;
+            if (c_row0 < M && x < N) tma_store_2d(tmap_c, staging + (c & 1) * kEpiBufBytes, x, c_row0);
+            bulk_commit_group();  // an empty group keeps the per-buffer accounting uniform
+        }
+    }
 }
 
 }  // namespace gemm103

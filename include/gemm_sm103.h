@@ -62,7 +62,7 @@ typedef enum {
 
 /* Tile configurations (TILE_M x TILE_N x TILE_K). */
 typedef enum {
-    GEMM_TILE_AUTO = 0,       /* the library picks (currently 128x256x64) */
+    GEMM_TILE_AUTO = 0,       /* the library picks: 256x256x64_PAIR when M > 128, else 128x256x64 */
     GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */
     GEMM_TILE_128x64x32 = 2,  /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
                                  BLOCK_SIZE_N 64, BLOCK_SIZE_K 32) */
@@ -106,7 +106,7 @@ int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int6
                           int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace, void* stream);
 
 /*
- * Tile shape a configuration uses for a problem: writes TILE_M, TILE_N,
+ * Tile shape a configuration uses for a problem (GEMM_TILE_AUTO depends on M): writes TILE_M, TILE_N,
  * TILE_K (host pointers, each may be NULL) and returns GEMM_OK, or
  * GEMM_ERR_UNSUPPORTED for an unknown tile_cfg. No device work.
  */
@@ -161,8 +161,8 @@ int gemm_set_fault_injection(int32_t mode);
 uint64_t gemm_launch_count(void);
 
 /*
- * gemm_f16_f32acc_noalloc -- the same GEMM as gemm_f16_f32acc (default tile
- * configuration), for callers that cannot allocate device memory when they
+ * gemm_f16_f32acc_noalloc -- the same GEMM as gemm_f16_f32acc, run with the
+ * one-CTA 128x256x64 tile, for callers that cannot allocate device memory when they
  * call it. The pages have no counterpart to this entry point: it exists for
  * callers such as code being captured into a CUDA graph (cudaMalloc is
  * refused during capture), inference-runtime plugins whose enqueue step must
