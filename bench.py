@@ -247,7 +247,7 @@ def run_ours(args, w, rank, world, local_rank):
     a, b = A.to(dev), B.to(dev)
     c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
     tm, tn, tk = g.tile_shape(args.tile_cfg, w.M, w.N, w.K)
-    tile = f"{tm}x{tn}x{tk}" + ("_pair" if tm == 256 else "")
+    tile = f"{tm}x{tn}x{tk}" + ("_pair" if tm == 256 else "")  # e.g. 256x256x128_pair
     kernel_name = "gemm_f16_f32acc_pair_kernel" if tm == 256 else "gemm_f16_f32acc_kernel"
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None

@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     TILE_128x64x32,
     TILE_128x256x64,
     TILE_256x256x64_PAIR,
+    TILE_256x256x128_PAIR,
     TILE_AUTO,
     GemmError,
     gemm,

@@ -25,6 +25,7 @@ TILE_AUTO = 0
 TILE_128x256x64 = 1
 TILE_128x64x32 = 2
 TILE_256x256x64_PAIR = 3
+TILE_256x256x128_PAIR = 4
 
 DEFAULT_GROUP_SIZE_M = 16
 

@@ -21,13 +21,14 @@ using namespace gemm103;
 using Cfg128x256 = TileCfg<128, 256, 64, 4>;
 using Cfg128x64 = TileCfg<128, 64, 32, 6>;
 using CfgPair256 = PairCfg<6>;
+using CfgPair256Deep = PairCfg<3, 128>;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumCfgs = 4;
+constexpr int kNumCfgs = 5;
 constexpr int64_t kMaxExtent = int64_t(1) << 30;
 constexpr uint64_t kDefaultWatchdogNs = 2000000000ull;
 
@@ -152,11 +153,12 @@ int validate(const Problem& pr)
     return GEMM_OK;
 }
 
-// GEMM_TILE_AUTO: the CTA-pair 256x256 tile unless the problem has at most
-// one 128-row band, where half of every pair tile would be empty.
+// GEMM_TILE_AUTO: the CTA-pair 256x256 tile with 128-deep k steps unless the
+// problem has at most one 128-row band, where half of every pair tile would
+// be empty.
 int resolve_cfg(int32_t tile_cfg, int64_t M, int32_t* tm, int32_t* tn, int32_t* tk)
 {
-    if (tile_cfg == GEMM_TILE_AUTO) tile_cfg = M > 128 ? GEMM_TILE_256x256x64_PAIR : GEMM_TILE_128x256x64;
+    if (tile_cfg == GEMM_TILE_AUTO) tile_cfg = M > 128 ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x256x64;
     switch (tile_cfg) {
         case GEMM_TILE_128x256x64:
             *tm = Cfg128x256::TM, *tn = Cfg128x256::TN, *tk = Cfg128x256::TK;
@@ -167,6 +169,9 @@ int resolve_cfg(int32_t tile_cfg, int64_t M, int32_t* tm, int32_t* tn, int32_t* 
         case GEMM_TILE_256x256x64_PAIR:
             *tm = CfgPair256::TM, *tn = CfgPair256::TN, *tk = CfgPair256::TK;
             return GEMM_TILE_256x256x64_PAIR;
+        case GEMM_TILE_256x256x128_PAIR:
+            *tm = CfgPair256Deep::TM, *tn = CfgPair256Deep::TN, *tk = CfgPair256Deep::TK;
+            return GEMM_TILE_256x256x128_PAIR;
         default:
             return -1;
     }
@@ -281,7 +286,7 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     rc = make_map(&mc, pr.C, pr.N, pr.M, pr.N, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc != GEMM_OK) return rc;
     if (pr.K > 0) {
-        rc = make_map(&ma, pr.A, pr.K, pr.M, pr.K, Cfg::TK, Cfg::CTA_M, CU_TENSOR_MAP_SWIZZLE_128B);
+        rc = make_map(&ma, pr.A, pr.K, pr.M, pr.K, 64, Cfg::CTA_M, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != GEMM_OK) return rc;
         rc = make_map(&mb, pr.B, pr.N, pr.K, pr.N, 64, Cfg::TK, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != GEMM_OK) return rc;
@@ -396,6 +401,8 @@ int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int6
             return launch<Cfg128x64>(pr, cfg, tile_trace, s);
         case GEMM_TILE_256x256x64_PAIR:
             return launch_pair<CfgPair256>(pr, cfg, tile_trace, s);
+        case GEMM_TILE_256x256x128_PAIR:
+            return launch_pair<CfgPair256Deep>(pr, cfg, tile_trace, s);
         default:
             return launch<Cfg128x256>(pr, cfg, tile_trace, s);
     }

@@ -11,14 +11,14 @@
 // (tile_map.cuh).
 //
 // GB300 mapping (one CTA of 192 threads per SM, persistent over tiles):
-//   warp 0, lane 0   TMA producer: per k step, one A box (TILE_K x TILE_M,
+//   warp 0           TMA producer (lane 0 issues): per k step, one A box (TILE_K x TILE_M,
 //                    K contiguous) and TILE_N/64 B boxes (64 x TILE_K, N
 //                    contiguous) into an S-stage shared-memory ring, tracked by
 //                    full/empty mbarriers. Loads past M, N or K are zero-filled
 //                    by the TMA unit, so edge tiles need no masking on load and
 //                    a partial last k step adds exact zeros.
 //   warp 1           allocates tensor memory (two TILE_N-column fp32
-//                    accumulators); lane 0 issues tcgen05.mma kind::f16
+//                    accumulators) and runs the MMA schedule; lane 0 issues tcgen05.mma kind::f16
 //                    (M=128, N=TILE_N, K=16), A K-major and B N-major straight
 //                    from the swizzled shared-memory tiles, and commits each
 //                    stage back to its empty barrier and each finished tile to
@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && p.num_k_tiles > 0 && p.fault_mode != 1) {
+        // The whole warp runs the schedule; lane 0 issues.
+        if (p.num_k_tiles > 0 && p.fault_mode != 1) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;  // per stage: ever issued / parity of the last issue
@@ -144,17 +145,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 const int32_t m0 = tc.pid_m * Cfg::TM;
                 const int32_t n0 = tc.pid_n * Cfg::TN;
                 for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
-                    if (!wait_phase(&empty[stage], phase ^ 1u, w, kWhereProducer)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_TX);
+                    ok = warp_wait_phase(&empty[stage], phase ^ 1u, w, kWhereProducer);
+                    if (!ok) break;
                     const int32_t k0 = kt * Cfg::TK;
-                    tma_load_2d(sA + stage * Cfg::A_STAGE, &tmap_a, &full[stage], k0, m0);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_TX);
+                        tma_load_2d(sA + stage * Cfg::A_STAGE, &tmap_a, &full[stage], k0, m0);
 #pragma unroll
-                    for (int j = 0; j < Cfg::TN / 64; ++j)
-                        tma_load_2d(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmap_b, &full[stage], n0 + 64 * j,
-                                    k0);
+                        for (int j = 0; j < Cfg::TN / 64; ++j)
+                            tma_load_2d(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmap_b, &full[stage],
+                                        n0 + 64 * j, k0);
+                    }
+                    __syncwarp();
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == Cfg::STAGES) {
@@ -163,14 +165,17 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     }
                 }
             }
-            if (!ok) {  // aborting: every load already issued lands before the CTA exits
+            if (!ok && lane == 0) {  // aborting: every load already issued lands before the CTA exits
                 for (int s = 0; s < Cfg::STAGES; ++s)
                     if (issued & (1u << s)) wait_phase_drain(&full[s], (issued_parity >> s) & 1u, w);
             }
+            __syncwarp();
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && p.num_k_tiles > 0) {
+        // The whole warp runs the schedule and computes the descriptors; lane 0
+        // issues the MMAs and the commits.
+        if (p.num_k_tiles > 0) {
             int stage = 0;
             uint32_t phase = 0;
             int buf = 0;
@@ -179,42 +184,49 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const uint32_t a_base = smem_addr(sA);
             const uint32_t b_base = smem_addr(sB);
             for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                if (!wait_phase(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma)) break;
+                ok = warp_wait_phase(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma);
+                if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::TN);
                 for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
-                    if (!wait_phase(&full[stage], phase, w, kWhereMma)) {
-                        ok = false;
-                        break;
-                    }
+                    ok = warp_wait_phase(&full[stage], phase, w, kWhereMma);
+                    if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t a_s = a_base + stage * Cfg::A_STAGE;
                     const uint32_t b_s = b_base + stage * Cfg::B_STAGE;
+                    uint64_t ad[Cfg::TK / 16], bd[Cfg::TK / 16];
 #pragma unroll
                     for (int kk = 0; kk < Cfg::TK / 16; ++kk) {
-                        const uint64_t ad = make_smem_desc(a_s + kk * Cfg::A_KSTEP, 16u, Cfg::A_SBO, Cfg::A_SWIZZLE);
-                        const uint64_t bd = make_smem_desc(b_s + kk * Cfg::B_KSTEP, Cfg::B_LBO, Cfg::B_SBO,
-                                                           kSwizzle128B);
-                        tc_mma_f16_ss(d_tmem, ad, bd, Cfg::IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+                        ad[kk] = make_smem_desc(a_s + kk * Cfg::A_KSTEP, 16u, Cfg::A_SBO, Cfg::A_SWIZZLE);
+                        bd[kk] = make_smem_desc(b_s + kk * Cfg::B_KSTEP, Cfg::B_LBO, Cfg::B_SBO, kSwizzle128B);
                     }
-                    tc_commit(&empty[stage]);  // frees the stage when these MMAs are done
+                    if (lane == 0) {
+#pragma unroll
+                        for (int kk = 0; kk < Cfg::TK / 16; ++kk)
+                            tc_mma_f16_ss(d_tmem, ad[kk], bd[kk], Cfg::IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(&empty[stage]);  // frees the stage when these MMAs are done
+                    }
+                    __syncwarp();
                     if (++stage == Cfg::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(&acc_full[buf]);  // accumulator complete
+                if (lane == 0) tc_commit(&acc_full[buf]);  // accumulator complete
+                __syncwarp();
                 if (++buf == 2) {
                     buf = 0;
                     acc_phase ^= 1u;
                 }
             }
             // every MMA issued above has finished before tensor memory is freed
-            tc_commit(drain);
-            wait_phase_drain(drain, 0u, w);
+            if (lane == 0) {
+                tc_commit(drain);
+                wait_phase_drain(drain, 0u, w);
+            }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access

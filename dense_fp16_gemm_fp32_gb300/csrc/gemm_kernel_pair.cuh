@@ -13,7 +13,7 @@
 //     k step for the same 128 x 256 x 64 of work that costs 48 KiB alone.
 //   * Both CTAs' TMA loads complete on the even CTA's full barrier, which the
 //     even CTA arms with the pair's total byte count.
-//   * One thread of the even CTA issues the MMAs and commits each stage to the
+//   * The even CTA's MMA warp runs the schedule; its lane 0 issues the MMAs and commits each stage to the
 //     empty barriers of both CTAs and each finished accumulator to the
 //     accumulator-full barriers of both CTAs (one commit per barrier, by its
 //     cluster address).
@@ -38,21 +38,27 @@
 
 namespace gemm103 {
 
-template <int STAGES_>
+// TK is the depth of one pipeline stage (64 or 128). A stage's A panel is
+// stored as TK/64 sub-tiles of 128 rows x 64 k (one 128-byte swizzle span per
+// row); its B panel as CTA_N/64 boxes of TK k rows x 64 columns. Deeper stages
+// amortise the per-stage wait, fence and commits over more MMAs.
+template <int STAGES_, int TK_ = 64>
 struct PairCfg {
-    static constexpr int TM = 256, TN = 256, TK = 64, STAGES = STAGES_;  // tile of the pair
+    static constexpr int TM = 256, TN = 256, TK = TK_, STAGES = STAGES_;  // tile of the pair
+    static_assert(TK == 64 || TK == 128, "stage depth of 64 or 128");
     static constexpr int CTA_M = 128;                                     // A / D rows per CTA
     static constexpr int CTA_N = 128;                                     // B columns per CTA
     static constexpr int NUM_THREADS = 192;
     static constexpr int EPI_WARPS = 4;
 
-    static constexpr int A_STAGE = CTA_M * TK * 2;        // 16 KiB
-    static constexpr int B_BOX = TK * 64 * 2;             // 8 KiB: 64 columns x TK rows
-    static constexpr int B_STAGE = (CTA_N / 64) * B_BOX;  // 16 KiB
+    static constexpr int A_SUB = CTA_M * 64 * 2;          // 16 KiB: 128 rows x 64 k
+    static constexpr int A_STAGE = (TK / 64) * A_SUB;
+    static constexpr int B_BOX = TK * 64 * 2;             // 64 columns x TK rows
+    static constexpr int B_STAGE = (CTA_N / 64) * B_BOX;
     static constexpr uint32_t PAIR_STAGE_TX = 2u * (A_STAGE + B_STAGE);
 
     static constexpr uint32_t A_SBO = 1024;       // 8 rows x 128 B
-    static constexpr uint32_t A_KSTEP = 32;       // 16 fp16 along K
+    static constexpr uint32_t A_KSTEP = 32;       // 16 fp16 along K inside a sub-tile
     static constexpr uint32_t B_LBO = B_BOX;      // next 64 columns
     static constexpr uint32_t B_SBO = 1024;       // next 8 k rows
     static constexpr uint32_t B_KSTEP = 16 * 128; // 16 k rows
@@ -126,7 +132,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
-        if (lane == 0 && p.num_k_tiles > 0 && p.fault_mode != 1) {
+        // The whole warp runs the schedule; lane 0 issues.
+        if (p.num_k_tiles > 0 && p.fault_mode != 1) {
             const uint32_t full0_even = map_shared_to_rank(smem_addr(&full[0]), 0);
             int stage = 0;
             uint32_t phase = 0;
@@ -136,17 +143,20 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 const int32_t m0 = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M;
                 const int32_t n0 = tc.pid_n * Cfg::TN + static_cast<int32_t>(rank) * Cfg::CTA_N;
                 for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
-                    if (!wait_phase<true>(&empty[stage], phase ^ 1u, w, kWhereProducer)) {
-                        ok = false;
-                        break;
-                    }
-                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], Cfg::PAIR_STAGE_TX);
+                    ok = warp_wait_phase<true>(&empty[stage], phase ^ 1u, w, kWhereProducer);
+                    if (!ok) break;
                     const uint32_t fb = full0_even + 8u * static_cast<uint32_t>(stage);
                     const int32_t k0 = kt * Cfg::TK;
-                    tma_load_2d_pair(sA + stage * Cfg::A_STAGE, &tmap_a, fb, k0, m0);
+                    if (lane == 0) {
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], Cfg::PAIR_STAGE_TX);
 #pragma unroll
-                    for (int j = 0; j < Cfg::CTA_N / 64; ++j)
-                        tma_load_2d_pair(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmap_b, fb, n0 + 64 * j, k0);
+                        for (int j = 0; j < Cfg::TK / 64; ++j)
+                            tma_load_2d_pair(sA + stage * Cfg::A_STAGE + j * Cfg::A_SUB, &tmap_a, fb, k0 + 64 * j, m0);
+#pragma unroll
+                        for (int j = 0; j < Cfg::CTA_N / 64; ++j)
+                            tma_load_2d_pair(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmap_b, fb, n0 + 64 * j, k0);
+                    }
+                    __syncwarp();
                     if (++stage == Cfg::STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -155,7 +165,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             }
             // every stage released: no commit from the MMA thread still targets this CTA
             for (int i = 0; ok && i < Cfg::STAGES; ++i) {
-                ok = wait_phase<true>(&empty[stage], phase ^ 1u, w, kWhereProducer);
+                ok = warp_wait_phase<true>(&empty[stage], phase ^ 1u, w, kWhereProducer);
                 if (++stage == Cfg::STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -164,7 +174,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
-        if (rank == 0 && lane == 0 && p.num_k_tiles > 0) {
+        // The whole warp runs the schedule and computes the descriptors; lane 0
+        // issues the MMAs and the commits (tcgen05.commit tracks the MMAs of the
+        // thread that issues it).
+        if (rank == 0 && p.num_k_tiles > 0) {
             int stage = 0;
             uint32_t phase = 0;
             int buf = 0;
@@ -177,38 +190,43 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const uint32_t accf0_even = map_shared_to_rank(smem_addr(&acc_full[0]), 0);
             const uint32_t accf0_odd = map_shared_to_rank(smem_addr(&acc_full[0]), 1);
             for (int32_t tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
-                if (!wait_phase<true>(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma)) {
-                    ok = false;
-                    break;
-                }
+                ok = warp_wait_phase<true>(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma);
+                if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * Cfg::ACC_COLS;
                 for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
-                    if (!wait_phase(&full[stage], phase, w, kWhereMma)) {
-                        ok = false;
-                        break;
-                    }
+                    ok = warp_wait_phase(&full[stage], phase, w, kWhereMma);
+                    if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t a_s = a_base + stage * Cfg::A_STAGE;
                     const uint32_t b_s = b_base + stage * Cfg::B_STAGE;
+                    uint64_t ad[Cfg::TK / 16], bd[Cfg::TK / 16];
 #pragma unroll
                     for (int kk = 0; kk < Cfg::TK / 16; ++kk) {
-                        const uint64_t ad = make_smem_desc(a_s + kk * Cfg::A_KSTEP, 16u, Cfg::A_SBO, kSwizzle128B);
-                        const uint64_t bd =
-                            make_smem_desc(b_s + kk * Cfg::B_KSTEP, Cfg::B_LBO, Cfg::B_SBO, kSwizzle128B);
-                        tc_mma_f16_ss_pair(d_tmem, ad, bd, Cfg::IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+                        ad[kk] = make_smem_desc(a_s + (kk / 4) * Cfg::A_SUB + (kk % 4) * Cfg::A_KSTEP, 16u, Cfg::A_SBO,
+                                                kSwizzle128B);
+                        bd[kk] = make_smem_desc(b_s + kk * Cfg::B_KSTEP, Cfg::B_LBO, Cfg::B_SBO, kSwizzle128B);
                     }
                     const uint32_t off = 8u * static_cast<uint32_t>(stage);
-                    tc_commit_pair(empty0_even + off);  // the stage is free in both CTAs
-                    tc_commit_pair(empty0_odd + off);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int kk = 0; kk < Cfg::TK / 16; ++kk)
+                            tc_mma_f16_ss_pair(d_tmem, ad[kk], bd[kk], Cfg::IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit_pair(empty0_even + off);  // the stage is free in both CTAs
+                        tc_commit_pair(empty0_odd + off);
+                    }
+                    __syncwarp();
                     if (++stage == Cfg::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit_pair(accf0_even + 8u * static_cast<uint32_t>(buf));  // accumulator complete
-                tc_commit_pair(accf0_odd + 8u * static_cast<uint32_t>(buf));
+                if (lane == 0) {
+                    tc_commit_pair(accf0_even + 8u * static_cast<uint32_t>(buf));  // accumulator complete
+                    tc_commit_pair(accf0_odd + 8u * static_cast<uint32_t>(buf));
+                }
+                __syncwarp();
                 if (++buf == 2) {
                     buf = 0;
                     acc_phase ^= 1u;
@@ -216,17 +234,19 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             }
             // both epilogues have released both accumulators: no arrive still targets this CTA
             for (int i = 0; ok && i < 2; ++i) {
-                ok = wait_phase<true>(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma);
+                ok = warp_wait_phase<true>(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma);
                 if (++buf == 2) {
                     buf = 0;
                     acc_phase ^= 1u;
                 }
             }
             // every MMA issued above has finished before tensor memory is freed
-            tc_commit_pair(map_shared_to_rank(smem_addr(drain), 0));
-            wait_phase_drain(drain, 0u, w);
+            if (lane == 0) {
+                tc_commit_pair(map_shared_to_rank(smem_addr(drain), 0));
+                wait_phase_drain(drain, 0u, w);
+            }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;

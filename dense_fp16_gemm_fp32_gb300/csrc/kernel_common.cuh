@@ -72,6 +72,19 @@ __device__ __forceinline__ void wait_phase_drain(uint64_t* bar, uint32_t parity,
     }
 }
 
+// wait_phase for a whole warp: every lane waits, and the result is made
+// warp-uniform. Keeping the producer and MMA schedules warp-uniform (all lanes
+// run the loops and compute the descriptors, one lane issues) lets the
+// compiler keep the tcgen05 operands in uniform registers; a loop whose trip
+// depends on one lane's wait results cannot, and the MMA issue rate drops to
+// about two thirds of the tensor-core rate.
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, const Watch& w, uint32_t where)
+{
+    const bool ok = wait_phase<kClusterScope>(bar, parity, w, where);
+    return __all_sync(0xffffffffu, ok) != 0;
+}
+
 __device__ __forceinline__ uint32_t pack_half2_rn(uint32_t lo_bits, uint32_t hi_bits)
 {
     const __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));

@@ -62,12 +62,13 @@ typedef enum {
 
 /* Tile configurations (TILE_M x TILE_N x TILE_K). */
 typedef enum {
-    GEMM_TILE_AUTO = 0,       /* the library picks: 256x256x64_PAIR when M > 128, else 128x256x64 */
+    GEMM_TILE_AUTO = 0,       /* the library picks: 256x256x128_PAIR when M > 128, else 128x256x64 */
     GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */
     GEMM_TILE_128x64x32 = 2,  /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
                                  BLOCK_SIZE_N 64, BLOCK_SIZE_K 32) */
-    GEMM_TILE_256x256x64_PAIR = 3 /* a 2-CTA cluster per tile (tcgen05 cta_group::2): each
+    GEMM_TILE_256x256x64_PAIR = 3, /* a 2-CTA cluster per tile (tcgen05 cta_group::2): each
                                  CTA stages 128 rows of A and 128 columns of B, 6 stages */
+    GEMM_TILE_256x256x128_PAIR = 4 /* as 3 with 128-deep k steps, 3 stages */
 } gemm_tile_cfg_t;
 
 /*

@@ -39,8 +39,9 @@ def test_status_strings(lib):
 
 def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_AUTO, M=128) == (128, 256, 64)
-    assert g.tile_shape(g.TILE_AUTO, M=129) == (256, 256, 64)
+    assert g.tile_shape(g.TILE_AUTO, M=129) == (256, 256, 128)
     assert g.tile_shape(g.TILE_256x256x64_PAIR) == (256, 256, 64)
+    assert g.tile_shape(g.TILE_256x256x128_PAIR) == (256, 256, 128)
     assert g.tile_shape(g.TILE_128x256x64) == (128, 256, 64)
     assert g.tile_shape(g.TILE_128x64x32) == (128, 64, 32)
     with pytest.raises(g.GemmError) as e:

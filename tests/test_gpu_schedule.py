@@ -57,6 +57,7 @@ def _kernel_trace(M, N, K, G, cfg, seed):
     (4095, 3000, 64, 5, g.TILE_128x256x64),    # ragged grid, clamped band
     (8192, 8192, 128, 8, g.TILE_256x256x64_PAIR),   # 1024 pair tiles over the resident clusters
     (4095, 3000, 64, 3, g.TILE_256x256x64_PAIR),
+    (4095, 3000, 1000, 4, g.TILE_256x256x128_PAIR),
     (896, 192, 64, 2, g.TILE_128x64x32),
 ])
 def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
@@ -69,7 +70,7 @@ def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
     # persistent schedule: CTA b processes pids b, b + grid, b + 2*grid, ...
     assert torch.equal(ctas, torch.arange(len(want), dtype=torch.int32) % grid)
     assert grid <= torch.cuda.get_device_properties(0).multi_processor_count * 4
-    if cfg == g.TILE_256x256x64_PAIR:
+    if cfg in (g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR):
         assert grid <= torch.cuda.get_device_properties(0).multi_processor_count // 2
     if M * N * K <= 1.3e10:
         check_against_oracle(A, B, C)
