@@ -152,6 +152,24 @@ class ClockSampler:
                 "window": window}
 
 
+# ---------------------------------------------------------------- ranks
+def max_over_ranks(ms: float, device, world: int) -> float:
+    """The slowest rank's time: every rank contributes its own, all receive the max."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Replicas: every rank runs `steps` steps; the job's rate is all ranks' flops
+    over the slowest rank's time."""
+    return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- CPU oracle
 def time_oracle(A, B, rows, nthreads):
     from oracle import gemm as og
@@ -294,10 +312,7 @@ def run_ours(args, w, rank, world, local_rank):
         total_ms = sum(per_launch_ms)
     else:
         total_ms = starts[0].elapsed_time(ends[-1])
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms_max = float(t.item())
+    total_ms_max = max_over_ranks(total_ms, dev, world)
 
     # ---- end to end through the public API from pinned host buffers
     e2e_ms, e2e_steps, e2e_mode = run_e2e(args, w, g, A, B, dev, world)
@@ -305,7 +320,7 @@ def run_ours(args, w, rank, world, local_rank):
     if rank != 0:
         return 0
     flops = 2.0 * w.M * w.N * w.K
-    value = flops * args.steps * world / (total_ms_max * 1e-3) / 1e12
+    value = whole_job_tflops(flops, args.steps, world, total_ms_max)
     kernel_ms = statistics.fmean(per_launch_ms)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
@@ -323,7 +338,7 @@ def run_ours(args, w, rank, world, local_rank):
                                     "fp16 and bf16 share the tensor rate",
                      "kernel": f"{kernel_name} {tile}", "kernel_ms": kernel_ms,
                      "flops_per_launch": flops},
-        "e2e": {"value": flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": whole_job_tflops(flops, e2e_steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": 2 * (w.M * w.K + w.K * w.N), "d2h_bytes_per_step": 2 * w.M * w.N,
                 "steps": e2e_steps, "mode": e2e_mode},
         "gpu_launches": launches,
@@ -393,10 +408,7 @@ def run_e2e(args, w, g, A, B, dev, world):
     s_out.wait_stream(s_gemm)
     e1.record(s_out)
     torch.cuda.synchronize(dev)
-    te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    return float(te.item()), steps, "pipelined: H2D, GEMM and D2H streams, 2 buffers"
+    return max_over_ranks(e0.elapsed_time(e1), dev, world), steps, "pipelined: H2D, GEMM and D2H streams, 2 buffers"
 
 
 def main():
@@ -406,7 +418,7 @@ def main():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="square8192")
-    p.add_argument("--group-size-m", type=int, default=16)
+    p.add_argument("--group-size-m", type=int, default=8)
     p.add_argument("--tile-cfg", type=int, default=0)
     p.add_argument("--flush-l2", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=50)

@@ -27,7 +27,7 @@ TILE_128x64x32 = 2
 TILE_256x256x64_PAIR = 3
 TILE_256x256x128_PAIR = 4
 
-DEFAULT_GROUP_SIZE_M = 16
+DEFAULT_GROUP_SIZE_M = 8
 
 HEADER = os.path.join(_build.ROOT, "include", "gemm_sm103.h")
 
