@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     header_functions,
     last_cuda_error,
     launch_count,
+    launch_plan,
     lib_path,
     load,
     query_status,

@@ -52,6 +52,8 @@ _SIGNATURES = {
     "gemm_tile_schedule": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_int32, _c_void_p, _c_void_p, _c_void_p]),
     "gemm_query_status": (ctypes.c_int, [_c_void_p]),
+    "gemm_launch_plan": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                        _c_void_p, _c_void_p, _c_void_p]),
     "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gemm_last_cuda_error": (ctypes.c_int, []),
     "gemm_set_watchdog_ns": (ctypes.c_int, [ctypes.c_uint64]),
@@ -164,6 +166,17 @@ def tile_shape(tile_cfg: int = TILE_AUTO, M: int = 0, N: int = 0, K: int = 0) ->
     _check(load().gemm_tile_shape(int(tile_cfg), M, N, K, ctypes.byref(tm), ctypes.byref(tn), ctypes.byref(tk)),
            "gemm_tile_shape")
     return tm.value, tn.value, tk.value
+
+
+def launch_plan(M: int, N: int, K: int = 0, tile_cfg: int = TILE_AUTO, device=None) -> dict:
+    """How the library schedules a problem on a device: grid CTAs, tiles, split tail tiles."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ctas, tiles, split = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    with torch.cuda.device(device):
+        rc = load().gemm_launch_plan(int(tile_cfg), M, N, K, ctypes.byref(ctas), ctypes.byref(tiles),
+                                     ctypes.byref(split))
+    _check(rc, "gemm_launch_plan")
+    return {"grid_ctas": ctas.value, "num_tiles": tiles.value, "split_tiles": split.value}
 
 
 def tile_schedule(M: int, N: int, tile_m: int, tile_n: int, group_size_m: int, device=None):

@@ -231,6 +231,8 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     p.trace = trace;
     p.watchdog_ns = watchdog_ns();
     p.fault_mode = g_fault_mode.load();
+    p.num_full_tiles = p.num_tiles;
+    p.num_units = p.num_tiles;
 
     const int64_t slots = static_cast<int64_t>(d->sm_count) * d->ctas_per_sm[cfg_id];
     const unsigned grid = static_cast<unsigned>(num_tiles < slots ? num_tiles : slots);
@@ -238,6 +240,53 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
+// Tiles of the last partial wave that the CTA-pair kernel computes as two
+// column halves: all of them when they would occupy at most half of the
+// resident clusters (then the halves fit in one wave), otherwise none.
+int64_t split_tail_tiles(int64_t num_tiles, int64_t clusters)
+{
+    if (clusters <= 0) return 0;
+    const int64_t rem = num_tiles % clusters;
+    return (rem > 0 && 2 * rem <= clusters) ? rem : 0;
+}
+
+cudaLaunchAttribute pair_cluster_attr()
+{
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    return attr;
+}
+
+// Resident clusters of a CTA-pair configuration on the current device (and
+// the kernel's shared-memory attribute), set up once per device.
+template <class Cfg>
+int pair_clusters(DeviceState* d, int cfg_id, int64_t* clusters)
+{
+    auto kernel = gemm_f16_f32acc_pair_kernel<Cfg>;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d->attr_set[cfg_id]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e);
+        cudaLaunchAttribute attr = pair_cluster_attr();
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(static_cast<unsigned>(2 * d->sm_count), 1, 1);
+        q.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
+        q.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        q.attrs = &attr;
+        q.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kernel, &q);
+        if (e != cudaSuccess) return cuda_fail(e);
+        d->ctas_per_sm[cfg_id] = n < 1 ? 1 : n;  // for pair configurations: resident clusters per device
+        d->attr_set[cfg_id] = true;
+    }
+    *clusters = d->ctas_per_sm[cfg_id];
     return GEMM_OK;
 }
 
@@ -250,29 +299,10 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     int rc = device_state(&d);
     if (rc != GEMM_OK) return rc;
     auto kernel = gemm_f16_f32acc_pair_kernel<Cfg>;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!d->attr_set[cfg_id]) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-            if (e != cudaSuccess) return cuda_fail(e);
-            cudaLaunchConfig_t q = {};
-            q.gridDim = dim3(static_cast<unsigned>(2 * d->sm_count), 1, 1);
-            q.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
-            q.dynamicSmemBytes = Cfg::SMEM_BYTES;
-            q.attrs = &attr;
-            q.numAttrs = 1;
-            int clusters = 0;
-            e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &q);
-            if (e != cudaSuccess) return cuda_fail(e);
-            d->ctas_per_sm[cfg_id] = clusters < 1 ? 1 : clusters;  // here: resident clusters per device
-            d->attr_set[cfg_id] = true;
-        }
-    }
+    cudaLaunchAttribute attr = pair_cluster_attr();
+    int64_t slots = 0;  // resident clusters
+    rc = pair_clusters<Cfg>(d, cfg_id, &slots);
+    if (rc != GEMM_OK) return rc;
 
     const int64_t num_pid_m = (pr.M + Cfg::TM - 1) / Cfg::TM;
     const int64_t num_pid_n = (pr.N + Cfg::TN - 1) / Cfg::TN;
@@ -307,8 +337,10 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     p.watchdog_ns = watchdog_ns();
     p.fault_mode = g_fault_mode.load();
 
-    const int64_t slots = d->ctas_per_sm[cfg_id];
-    const int64_t pairs = num_tiles < slots ? num_tiles : slots;
+    const int64_t split = split_tail_tiles(num_tiles, slots);
+    p.num_full_tiles = static_cast<int32_t>(num_tiles - split);
+    p.num_units = static_cast<int32_t>(num_tiles + split);
+    const int64_t pairs = p.num_units < slots ? p.num_units : slots;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     lc.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
@@ -426,6 +458,39 @@ int gemm_tile_shape(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* 
     return GEMM_OK;
 }
 
+int gemm_launch_plan(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* grid_ctas, int32_t* num_tiles,
+                     int32_t* split_tiles)
+{
+    (void)K;
+    int32_t tm, tn, tk;
+    const int cfg = resolve_cfg(tile_cfg, M, &tm, &tn, &tk);
+    if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
+    if (M < 0 || N < 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t tiles = ((M + tm - 1) / tm) * ((N + tn - 1) / tn);
+    if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != GEMM_OK) return rc;
+    int64_t ctas = 0, split = 0;
+    if (cfg == GEMM_TILE_256x256x64_PAIR || cfg == GEMM_TILE_256x256x128_PAIR) {
+        int64_t clusters = 0;
+        rc = cfg == GEMM_TILE_256x256x64_PAIR ? pair_clusters<CfgPair256>(d, cfg, &clusters)
+                                              : pair_clusters<CfgPair256Deep>(d, cfg, &clusters);
+        if (rc != GEMM_OK) return rc;
+        split = split_tail_tiles(tiles, clusters);
+        const int64_t units = tiles + split;
+        ctas = 2 * (units < clusters ? units : clusters);
+    } else {
+        // one-CTA kernels: occupancy is set up on first launch; report the SM bound
+        const int64_t slots = static_cast<int64_t>(d->sm_count) * (d->attr_set[cfg] ? d->ctas_per_sm[cfg] : 1);
+        ctas = tiles < slots ? tiles : slots;
+    }
+    if (grid_ctas) *grid_ctas = static_cast<int32_t>(ctas);
+    if (num_tiles) *num_tiles = static_cast<int32_t>(tiles);
+    if (split_tiles) *split_tiles = static_cast<int32_t>(split);
+    return GEMM_OK;
+}
+
 int gemm_tile_schedule(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n, int32_t group_size_m, int32_t* d_pid_m,
                        int32_t* d_pid_n, void* stream)
 {
@@ -539,6 +604,8 @@ int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, in
     p.trace = nullptr;
     p.watchdog_ns = watchdog_ns();
     p.fault_mode = 0;
+    p.num_full_tiles = p.num_tiles;
+    p.num_units = p.num_tiles;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The scratch keeps the previous call's contents: the status word starts at zero.

@@ -23,6 +23,10 @@
 //     the even CTA's accumulator-empty barrier as soon as its reads are done.
 //   * Tensor memory (2 x 256 fp32 columns, double buffered) is allocated and
 //     freed by one warp of each CTA together (cta_group::2).
+// Tail: when the last partial wave of tiles would leave more than half of the
+// clusters idle, the host marks those last pids as split; each is computed as
+// two 256 x 128 column halves (N = 128 MMAs) by two clusters, so the last wave
+// takes about half a tile's time. No partial sums cross CTAs.
 // Waits are bounded as in gemm_kernel.cuh. Before a CTA may exit, its
 // producer waits until every stage has been released (so no commit still
 // targets it) and the MMA thread waits until both epilogues have released
@@ -64,6 +68,9 @@ struct PairCfg {
     static constexpr uint32_t B_KSTEP = 16 * 128; // 16 k rows
 
     static constexpr uint32_t IDESC = make_idesc_f16_f32acc(TM, TN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+    // a column half of a tile (the split tail): N = 128, one 64-column B box per CTA
+    static constexpr uint32_t IDESC_HALF = make_idesc_f16_f32acc(TM, TN / 2, false, true);
+    static constexpr uint32_t PAIR_STAGE_TX_HALF = 2u * (A_STAGE + B_STAGE / 2);
     static constexpr uint32_t ACC_COLS = TN;      // one accumulator: 128 lanes x 256 fp32 columns per CTA
     static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 
@@ -73,6 +80,29 @@ struct PairCfg {
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
     static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
 };
+
+// Work unit u of the persistent schedule: the full tiles in pid order, then
+// the two column halves of each pid in [num_full_tiles, num_tiles), pid by pid.
+struct PairUnit {
+    TileCoord tc;
+    int32_t pid;
+    int32_t half;  // -1: the whole 256-column tile; 0 / 1: columns [0,128) / [128,256)
+};
+
+__device__ __forceinline__ PairUnit pair_unit(int32_t u, const GemmParams& p)
+{
+    PairUnit r;
+    if (u < p.num_full_tiles) {
+        r.pid = u;
+        r.half = -1;
+    } else {
+        const int32_t v = u - p.num_full_tiles;
+        r.pid = p.num_full_tiles + (v >> 1);
+        r.half = v & 1;
+    }
+    r.tc = grouped_tile(r.pid, p.num_pid_m, p.num_pid_n, p.group_size_m);
+    return r;
+}
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
@@ -138,22 +168,26 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int32_t tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
-                const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
-                const int32_t m0 = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M;
-                const int32_t n0 = tc.pid_n * Cfg::TN + static_cast<int32_t>(rank) * Cfg::CTA_N;
+            for (int32_t u = pair; ok && u < p.num_units; u += num_pairs) {
+                const PairUnit un = pair_unit(u, p);
+                const int32_t m0 = un.tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M;
+                // whole tile: this CTA's 128 of 256 columns; half tile: its 64 of the half's 128
+                const int32_t n0 = un.half < 0 ? un.tc.pid_n * Cfg::TN + static_cast<int32_t>(rank) * Cfg::CTA_N
+                                               : un.tc.pid_n * Cfg::TN + un.half * (Cfg::TN / 2) +
+                                                     static_cast<int32_t>(rank) * (Cfg::CTA_N / 2);
+                const int nbox = un.half < 0 ? Cfg::CTA_N / 64 : Cfg::CTA_N / 128;
+                const uint32_t tx = un.half < 0 ? Cfg::PAIR_STAGE_TX : Cfg::PAIR_STAGE_TX_HALF;
                 for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
                     ok = warp_wait_phase<true>(&empty[stage], phase ^ 1u, w, kWhereProducer);
                     if (!ok) break;
                     const uint32_t fb = full0_even + 8u * static_cast<uint32_t>(stage);
                     const int32_t k0 = kt * Cfg::TK;
                     if (lane == 0) {
-                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], Cfg::PAIR_STAGE_TX);
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
 #pragma unroll
                         for (int j = 0; j < Cfg::TK / 64; ++j)
                             tma_load_2d_pair(sA + stage * Cfg::A_STAGE + j * Cfg::A_SUB, &tmap_a, fb, k0 + 64 * j, m0);
-#pragma unroll
-                        for (int j = 0; j < Cfg::CTA_N / 64; ++j)
+                        for (int j = 0; j < nbox; ++j)
                             tma_load_2d_pair(sB + stage * Cfg::B_STAGE + j * Cfg::B_BOX, &tmap_b, fb, n0 + 64 * j, k0);
                     }
                     __syncwarp();
@@ -189,7 +223,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const uint32_t empty0_odd = map_shared_to_rank(smem_addr(&empty[0]), 1);
             const uint32_t accf0_even = map_shared_to_rank(smem_addr(&acc_full[0]), 0);
             const uint32_t accf0_odd = map_shared_to_rank(smem_addr(&acc_full[0]), 1);
-            for (int32_t tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
+            for (int32_t u = pair; ok && u < p.num_units; u += num_pairs) {
+                const uint32_t idesc = u < p.num_full_tiles ? Cfg::IDESC : Cfg::IDESC_HALF;
                 ok = warp_wait_phase<true>(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma);
                 if (!ok) break;
                 tc_fence_after_sync();
@@ -211,7 +246,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     if (lane == 0) {
 #pragma unroll
                         for (int kk = 0; kk < Cfg::TK / 16; ++kk)
-                            tc_mma_f16_ss_pair(d_tmem, ad[kk], bd[kk], Cfg::IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+                            tc_mma_f16_ss_pair(d_tmem, ad[kk], bd[kk], idesc, (kt > 0 || kk > 0) ? 1u : 0u);
                         tc_commit_pair(empty0_even + off);  // the stage is free in both CTAs
                         tc_commit_pair(empty0_odd + off);
                     }
@@ -254,19 +289,21 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const uint32_t acc_empty0_even = map_shared_to_rank(smem_addr(&acc_empty[0]), 0);
         int buf = 0;
         uint32_t acc_phase = 0;
-        for (int32_t tile = pair; tile < p.num_tiles; tile += num_pairs) {
-            const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
-            if (p.trace != nullptr && rank == 0 && warp == 2 && lane == 0) {
-                p.trace[3 * static_cast<int64_t>(tile) + 0] = tc.pid_m;
-                p.trace[3 * static_cast<int64_t>(tile) + 1] = tc.pid_n;
-                p.trace[3 * static_cast<int64_t>(tile) + 2] = pair;
+        for (int32_t u = pair; u < p.num_units; u += num_pairs) {
+            const PairUnit un = pair_unit(u, p);
+            const TileCoord tc = un.tc;
+            if (p.trace != nullptr && un.half <= 0 && rank == 0 && warp == 2 && lane == 0) {
+                p.trace[3 * static_cast<int64_t>(un.pid) + 0] = tc.pid_m;
+                p.trace[3 * static_cast<int64_t>(un.pid) + 1] = tc.pid_n;
+                p.trace[3 * static_cast<int64_t>(un.pid) + 2] = pair;
             }
             const int32_t gm = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + row;
-            const int32_t n0 = tc.pid_n * Cfg::TN;
+            const int32_t n0 = tc.pid_n * Cfg::TN + (un.half > 0 ? Cfg::TN / 2 : 0);
+            const int32_t ncols = un.half < 0 ? Cfg::TN : Cfg::TN / 2;
             uint16_t* crow = p.C + static_cast<size_t>(gm) * static_cast<size_t>(p.N);
             if (p.num_k_tiles == 0) {  // K == 0: the empty sum
                 if (gm < p.M) {
-                    for (int32_t c = 0; c < Cfg::TN; c += 8)
+                    for (int32_t c = 0; c < ncols; c += 8)
                         if (n0 + c < p.N) *reinterpret_cast<uint4*>(crow + n0 + c) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 continue;
@@ -278,13 +315,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const uint32_t t_row =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf) * Cfg::ACC_COLS;
             const uint32_t release_addr = acc_empty0_even + 8u * static_cast<uint32_t>(buf);
-            epilogue_tma_store<Cfg::TN>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c,
-                                        tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + q * 32, n0,
-                                        p.M, p.N, lane, [&]() {
-                                            tc_fence_before_sync();
-                                            __syncwarp();
-                                            if (lane == 0) mbar_arrive_cluster(release_addr);
-                                        });
+            const auto release = [&]() {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(release_addr);
+            };
+            const int32_t c_row0 = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + q * 32;
+            if (un.half < 0)
+                epilogue_tma_store<Cfg::TN>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c, c_row0, n0, p.M,
+                                            p.N, lane, release);
+            else
+                epilogue_tma_store<Cfg::TN / 2>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c, c_row0, n0,
+                                                p.M, p.N, lane, release);
             if (++buf == 2) {
                 buf = 0;
                 acc_phase ^= 1u;

@@ -24,6 +24,10 @@ struct GemmParams {
     int32_t* trace;  // NULL or 3 * num_tiles entries
     uint64_t watchdog_ns;
     int32_t fault_mode;  // 1: the producer issues nothing (watchdog test)
+    // CTA-pair kernel only: pids [num_full_tiles, num_tiles) are computed as two
+    // column halves each; work units are the full tiles followed by the halves.
+    int32_t num_full_tiles;
+    int32_t num_units;
 };
 
 struct Watch {

@@ -100,7 +100,8 @@ int gemm_f16_f32acc(const void* A, const void* B, void* C, int64_t M, int64_t N,
  *                the kernel's scheduler writes, for every pid it processes,
  *                tile_trace[3*pid + 0] = pid_m, [3*pid + 1] = pid_n,
  *                [3*pid + 2] = the CTA (blockIdx.x) that processed it, or for
- *                GEMM_TILE_256x256x64_PAIR the cluster (blockIdx.x / 2).
+ *                the CTA-pair configurations the cluster (blockIdx.x / 2) that
+ *                processed it (for a split tail tile: its first column half).
  *                Used to check the kernel's own order against the integer map.
  */
 int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
@@ -113,6 +114,24 @@ int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int6
  */
 int gemm_tile_shape(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tile_m,
                     int32_t* tile_n, int32_t* tile_k);
+
+/*
+ * How the current device would schedule a problem (no kernel launch):
+ *   grid_ctas    CTAs of the persistent grid (2 per cluster for the CTA-pair
+ *                configurations)
+ *   num_tiles    output tiles (program ids)
+ *   split_tiles  CTA-pair configurations: how many of the last pids are
+ *                computed as two 256 x 128 column halves by two clusters. The
+ *                persistent schedule runs units u = cluster, cluster + clusters,
+ *                ...: unit u < num_tiles - split_tiles is pid u; the remaining
+ *                units are the halves of the last split_tiles pids, two per pid
+ *                in pid order. A last wave of R tiles is split when 2R fits in
+ *                one wave of clusters.
+ * Host pointers, each may be NULL. Sets up the configuration's per-device
+ * state on first use (like a launch). GEMM_ERR_CUDA without a device.
+ */
+int gemm_launch_plan(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* grid_ctas, int32_t* num_tiles,
+                     int32_t* split_tiles);
 
 /*
  * The grouped pid -> (pid_m, pid_n) map, evaluated on the device by the same

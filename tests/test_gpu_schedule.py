@@ -55,9 +55,12 @@ def _kernel_trace(M, N, K, G, cfg, seed):
     (1024, 768, 128, 2, g.TILE_128x64x32),     # the worked example, 96 programs
     (8192, 8192, 256, 8, g.TILE_128x256x64),   # 2048 tiles: many per CTA
     (4095, 3000, 64, 5, g.TILE_128x256x64),    # ragged grid, clamped band
-    (8192, 8192, 128, 8, g.TILE_256x256x64_PAIR),   # 1024 pair tiles over the resident clusters
+    (8192, 8192, 128, 8, g.TILE_256x256x64_PAIR),   # 1024 pair tiles, split tail on 76 clusters
     (4095, 3000, 64, 3, g.TILE_256x256x64_PAIR),
     (4095, 3000, 1000, 4, g.TILE_256x256x128_PAIR),
+    (8192, 8192, 256, 8, g.TILE_256x256x128_PAIR),
+    (512, 1024, 256, 2, g.TILE_256x256x128_PAIR),    # 8 tiles: every tile split
+    (2048, 4096, 256, 3, g.TILE_256x256x128_PAIR),
     (896, 192, 64, 2, g.TILE_128x64x32),
 ])
 def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
@@ -66,11 +69,26 @@ def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
     got = [(int(a), int(b)) for a, b in tr[:, :2].tolist()]
     assert got == want                      # every pid processed once, with the oracle's tile
     ctas = tr[:, 2]
-    grid = int(ctas.max()) + 1
-    # persistent schedule: CTA b processes pids b, b + grid, b + 2*grid, ...
-    assert torch.equal(ctas, torch.arange(len(want), dtype=torch.int32) % grid)
-    assert grid <= torch.cuda.get_device_properties(0).multi_processor_count * 4
+    plan = g.launch_plan(M, N, K, tile_cfg=cfg)
+    assert plan["num_tiles"] == len(want)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     if cfg in (g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR):
-        assert grid <= torch.cuda.get_device_properties(0).multi_processor_count // 2
+        clusters = plan["grid_ctas"] // 2
+        assert 1 <= clusters <= sms // 2
+        split = plan["split_tiles"]
+        full = len(want) - split
+        units = full + 2 * split
+        if units > clusters:  # the grid is every resident cluster: the split rule applies
+            rem = len(want) % clusters
+            assert split == (rem if 0 < 2 * rem <= clusters else 0)
+        # persistent schedule over units: the full tiles, then two halves per split pid
+        pid = torch.arange(len(want))
+        first_unit = torch.where(pid < full, pid, full + 2 * (pid - full))
+        assert torch.equal(ctas.long(), first_unit % clusters)
+    else:
+        grid = int(ctas.max()) + 1
+        # persistent schedule: CTA b processes pids b, b + grid, b + 2*grid, ...
+        assert torch.equal(ctas, torch.arange(len(want), dtype=torch.int32) % grid)
+        assert grid <= sms * 4
     if M * N * K <= 1.3e10:
         check_against_oracle(A, B, C)
