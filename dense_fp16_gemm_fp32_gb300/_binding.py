@@ -47,6 +47,9 @@ _SIGNATURES = {
     "gemm_f16_f32acc_tiled": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _c_void_p,
                                              _c_void_p]),
+    "gemm_f16_f32acc_strided": (ctypes.c_int, [_c_void_p, ctypes.c_int64, _c_void_p, ctypes.c_int64, _c_void_p,
+                                               ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                               ctypes.c_int32, ctypes.c_int32, _c_void_p, _c_void_p]),
     "gemm_tile_shape": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                        _c_void_p, _c_void_p, _c_void_p]),
     "gemm_tile_schedule": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
@@ -119,8 +122,24 @@ def _check_operand(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be on a CUDA device, got {t.device}")
     if t.dim() != 2:
         raise ValueError(f"{name} must be 2-D, got shape {tuple(t.shape)}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous (row-major)")
+    if not _row_major(t):
+        raise ValueError(f"{name} must be row-major: unit column stride and a row stride >= its columns")
+
+
+def _row_major(t: torch.Tensor) -> bool:
+    """Row-major, possibly with padded rows: stride (ld, 1) with ld >= columns."""
+    rows, cols = t.shape
+    if rows <= 1 or cols <= 1:
+        return t.is_contiguous() or (t.stride(1) == 1 or cols <= 1)
+    return t.stride(1) == 1 and t.stride(0) >= cols
+
+
+def _ld(t: torch.Tensor) -> int:
+    """Row pitch in elements. A one-row tensor's pitch is never used to
+    address memory, so it is reported as its row length rounded up to 8."""
+    if t.shape[0] > 1:
+        return int(t.stride(0))
+    return max(8, -(-int(t.shape[1]) // 8) * 8)
 
 
 def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZE_M,
@@ -128,8 +147,11 @@ def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZ
          trace: torch.Tensor | None = None) -> torch.Tensor:
     """C = a @ b with fp16 operands, fp32 accumulation and one fp16 rounding.
 
-    a: [M,K] fp16 CUDA contiguous; b: [K,N] fp16 CUDA contiguous, same device.
-    out: optional [M,N] fp16 CUDA contiguous tensor to write.
+    a: [M,K] fp16 CUDA row-major; b: [K,N] fp16 CUDA row-major, same device.
+    Row-major views with padded rows (stride (ld, 1), ld >= columns) are
+    accepted; row pitches must then be multiples of 8 elements.
+    out: optional [M,N] fp16 CUDA row-major tensor (or padded view) to write;
+    its padding columns are not touched.
     trace: optional int32 CUDA tensor of 3 * num_tiles entries that receives
     (pid_m, pid_n, cta) per program id, as the kernel's scheduler ran them.
     Runs on the current CUDA stream of a's device.
@@ -155,9 +177,10 @@ def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZ
         trace_ptr = trace.data_ptr()
     lib = load()
     with torch.cuda.device(a.device):
-        rc = lib.gemm_f16_f32acc_tiled(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K,
-                                       int(group_size_m), int(tile_cfg), trace_ptr, _stream_ptr(a.device))
-    _check(rc, "gemm_f16_f32acc_tiled")
+        rc = lib.gemm_f16_f32acc_strided(a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(), _ld(out),
+                                         M, N, K, int(group_size_m), int(tile_cfg), trace_ptr,
+                                         _stream_ptr(a.device))
+    _check(rc, "gemm_f16_f32acc_strided")
     return out
 
 

@@ -130,6 +130,7 @@ struct Problem {
     void* C;
     int64_t M, N, K;
     int32_t group_size_m;
+    int64_t lda, ldb, ldc;  // row pitches in elements
 };
 
 int validate(const Problem& pr)
@@ -138,15 +139,21 @@ int validate(const Problem& pr)
     if (pr.M > kMaxExtent || pr.N > kMaxExtent || pr.K > kMaxExtent) return GEMM_ERR_UNSUPPORTED;
     if (pr.M == 0 || pr.N == 0) return GEMM_OK;
     if (pr.C == nullptr || (pr.K > 0 && (pr.A == nullptr || pr.B == nullptr))) return GEMM_ERR_INVALID_ARG;
+    // a row pitch covers its row
+    if (pr.ldc < pr.N || (pr.K > 0 && (pr.lda < pr.K || pr.ldb < pr.N))) return GEMM_ERR_INVALID_ARG;
+    if (pr.ldc > kMaxExtent || pr.lda > kMaxExtent || pr.ldb > kMaxExtent) return GEMM_ERR_UNSUPPORTED;
     const uintptr_t a = reinterpret_cast<uintptr_t>(pr.A), b = reinterpret_cast<uintptr_t>(pr.B),
                     c = reinterpret_cast<uintptr_t>(pr.C);
-    if ((c & 15u) != 0 || (pr.K > 0 && ((a & 15u) != 0 || (b & 15u) != 0))) return GEMM_ERR_UNSUPPORTED;
-    if ((pr.N & 7) != 0 || (pr.K & 7) != 0) return GEMM_ERR_UNSUPPORTED;
-    // C must not overlap A or B
-    const unsigned __int128 c_end = static_cast<unsigned __int128>(c) + static_cast<unsigned __int128>(pr.M) * pr.N * 2;
+    // TMA: 16-byte aligned bases and row pitches that are multiples of 16 bytes
+    if ((c & 15u) != 0 || (pr.ldc & 7) != 0) return GEMM_ERR_UNSUPPORTED;
+    if (pr.K > 0 && ((a & 15u) != 0 || (b & 15u) != 0 || (pr.lda & 7) != 0 || (pr.ldb & 7) != 0))
+        return GEMM_ERR_UNSUPPORTED;
+    // C must not overlap A or B (byte ranges spanned by the pitched rows)
+    using u128 = unsigned __int128;
+    const u128 c_end = static_cast<u128>(c) + (static_cast<u128>(pr.M - 1) * pr.ldc + pr.N) * 2;
     if (pr.K > 0) {
-        const unsigned __int128 a_end = static_cast<unsigned __int128>(a) + static_cast<unsigned __int128>(pr.M) * pr.K * 2;
-        const unsigned __int128 b_end = static_cast<unsigned __int128>(b) + static_cast<unsigned __int128>(pr.K) * pr.N * 2;
+        const u128 a_end = static_cast<u128>(a) + (static_cast<u128>(pr.M - 1) * pr.lda + pr.K) * 2;
+        const u128 b_end = static_cast<u128>(b) + (static_cast<u128>(pr.K - 1) * pr.ldb + pr.N) * 2;
         if (c < a_end && a < c_end) return GEMM_ERR_INVALID_ARG;
         if (c < b_end && b < c_end) return GEMM_ERR_INVALID_ARG;
     }
@@ -207,18 +214,19 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
     // C: 32 x 32 store boxes, 64-byte swizzle (matches the epilogue staging layout)
-    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.N, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc != GEMM_OK) return rc;
     if (pr.K > 0) {
         const CUtensorMapSwizzle a_swz = Cfg::TK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-        rc = make_map(&ma, pr.A, pr.K, pr.M, pr.K, Cfg::TK, Cfg::TM, a_swz);
+        rc = make_map(&ma, pr.A, pr.K, pr.M, pr.lda, Cfg::TK, Cfg::TM, a_swz);
         if (rc != GEMM_OK) return rc;
-        rc = make_map(&mb, pr.B, pr.N, pr.K, pr.N, 64, Cfg::TK, CU_TENSOR_MAP_SWIZZLE_128B);
+        rc = make_map(&mb, pr.B, pr.N, pr.K, pr.ldb, 64, Cfg::TK, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != GEMM_OK) return rc;
     }
 
     GemmParams p;
     p.C = static_cast<uint16_t*>(pr.C);
+    p.ldc = pr.ldc;
     p.M = static_cast<int32_t>(pr.M);
     p.N = static_cast<int32_t>(pr.N);
     p.K = static_cast<int32_t>(pr.K);
@@ -313,17 +321,18 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
     // C: 32 x 32 store boxes, 64-byte swizzle (matches the epilogue staging layout)
-    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.N, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc != GEMM_OK) return rc;
     if (pr.K > 0) {
-        rc = make_map(&ma, pr.A, pr.K, pr.M, pr.K, 64, Cfg::CTA_M, CU_TENSOR_MAP_SWIZZLE_128B);
+        rc = make_map(&ma, pr.A, pr.K, pr.M, pr.lda, 64, Cfg::CTA_M, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != GEMM_OK) return rc;
-        rc = make_map(&mb, pr.B, pr.N, pr.K, pr.N, 64, Cfg::TK, CU_TENSOR_MAP_SWIZZLE_128B);
+        rc = make_map(&mb, pr.B, pr.N, pr.K, pr.ldb, 64, Cfg::TK, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != GEMM_OK) return rc;
     }
 
     GemmParams p;
     p.C = static_cast<uint16_t*>(pr.C);
+    p.ldc = pr.ldc;
     p.M = static_cast<int32_t>(pr.M);
     p.N = static_cast<int32_t>(pr.N);
     p.K = static_cast<int32_t>(pr.K);
@@ -418,10 +427,11 @@ int noalloc_setup(NoAllocDeviceState** out)
 
 extern "C" {
 
-int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                          int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace, void* stream)
+int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t M,
+                            int64_t N, int64_t K, int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace,
+                            void* stream)
 {
-    const Problem pr{A, B, C, M, N, K, group_size_m};
+    const Problem pr{A, B, C, M, N, K, group_size_m, lda, ldb, ldc};
     int32_t tm, tn, tk;
     const int cfg = resolve_cfg(tile_cfg, M, &tm, &tn, &tk);
     if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
@@ -438,6 +448,12 @@ int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int6
         default:
             return launch<Cfg128x256>(pr, cfg, tile_trace, s);
     }
+}
+
+int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                          int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace, void* stream)
+{
+    return gemm_f16_f32acc_strided(A, K, B, N, C, N, M, N, K, group_size_m, tile_cfg, tile_trace, stream);
 }
 
 int gemm_f16_f32acc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int32_t group_size_m,
@@ -564,7 +580,7 @@ uint64_t gemm_launch_count(void) { return g_launches.load(); }
 int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                             int32_t group_size_m, uint32_t* d_status, void* stream)
 {
-    const Problem pr{A, B, C, M, N, K, group_size_m};
+    const Problem pr{A, B, C, M, N, K, group_size_m, K, N, N};
     int rc = validate(pr);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
     if (noalloc_scratch_words_needed() > kNoAllocScratchWords) return GEMM_ERR_UNSUPPORTED;
@@ -592,6 +608,7 @@ int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, in
 
     GemmParams p;
     p.C = static_cast<uint16_t*>(C);
+    p.ldc = N;
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);

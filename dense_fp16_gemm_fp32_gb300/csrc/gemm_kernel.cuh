@@ -242,12 +242,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             }
             const int32_t gm = tc.pid_m * Cfg::TM + row;
             const int32_t n0 = tc.pid_n * Cfg::TN;
-            uint16_t* crow = p.C + static_cast<size_t>(gm) * static_cast<size_t>(p.N);
+            uint16_t* crow = p.C + static_cast<int64_t>(gm) * p.ldc;
             if (p.num_k_tiles == 0) {  // K == 0: the empty sum
-                if (gm < p.M) {
-                    for (int32_t c = 0; c < Cfg::TN; c += 8)
-                        if (n0 + c < p.N) *reinterpret_cast<uint4*>(crow + n0 + c) = make_uint4(0u, 0u, 0u, 0u);
-                }
+                if (gm < p.M) store_zero_row(crow, n0, Cfg::TN, p.N);
                 continue;
             }
             bool ok = wait_phase(&acc_full[buf], acc_phase, w, kWhereEpilogue);
@@ -257,7 +254,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::TN);
             uint64_t* release_bar = &acc_empty[buf];
             epilogue_tma_store<Cfg::TN>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c,
-                                        tc.pid_m * Cfg::TM + q * 32, n0, p.M, p.N, lane, [&]() {
+                                        tc.pid_m * Cfg::TM + q * 32, n0, p.M, p.N, p.C, p.ldc, lane, [&]() {
                                             tc_fence_before_sync();
                                             __syncwarp();
                                             if (lane == 0) mbar_arrive(release_bar);

@@ -300,12 +300,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const int32_t gm = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + row;
             const int32_t n0 = tc.pid_n * Cfg::TN + (un.half > 0 ? Cfg::TN / 2 : 0);
             const int32_t ncols = un.half < 0 ? Cfg::TN : Cfg::TN / 2;
-            uint16_t* crow = p.C + static_cast<size_t>(gm) * static_cast<size_t>(p.N);
+            uint16_t* crow = p.C + static_cast<int64_t>(gm) * p.ldc;
             if (p.num_k_tiles == 0) {  // K == 0: the empty sum
-                if (gm < p.M) {
-                    for (int32_t c = 0; c < ncols; c += 8)
-                        if (n0 + c < p.N) *reinterpret_cast<uint4*>(crow + n0 + c) = make_uint4(0u, 0u, 0u, 0u);
-                }
+                if (gm < p.M) store_zero_row(crow, n0, ncols, p.N);
                 continue;
             }
             bool ok = wait_phase<true>(&acc_full[buf], acc_phase, w, kWhereEpilogue);
@@ -323,10 +320,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const int32_t c_row0 = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + q * 32;
             if (un.half < 0)
                 epilogue_tma_store<Cfg::TN>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c, c_row0, n0, p.M,
-                                            p.N, lane, release);
+                                            p.N, p.C, p.ldc, lane, release);
             else
                 epilogue_tma_store<Cfg::TN / 2>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c, c_row0, n0,
-                                                p.M, p.N, lane, release);
+                                                p.M, p.N, p.C, p.ldc, lane, release);
             if (++buf == 2) {
                 buf = 0;
                 acc_phase ^= 1u;

@@ -16,7 +16,8 @@ enum : uint32_t { kStatusTimeout = 1u };
 enum : uint32_t { kWhereProducer = 1u, kWhereMma = 2u, kWhereEpilogue = 3u, kWhereDrain = 4u };
 
 struct GemmParams {
-    uint16_t* C;  // fp16 bits, [M,N] row-major
+    uint16_t* C;  // fp16 bits, row i at C + i * ldc
+    int64_t ldc;  // row pitch of C in elements (a multiple of 8)
     int32_t M, N, K;
     int32_t num_pid_m, num_pid_n, num_tiles, num_k_tiles;
     int32_t group_size_m;  // already clamped to [1, num_pid_m]
@@ -89,6 +90,20 @@ __device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, 
     return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// C[row, n0 .. n0 + ncols) = +0 for the columns below N (the K == 0 case).
+// crow + n0 is 16-byte aligned; no element at or past column N is written.
+__device__ __forceinline__ void store_zero_row(uint16_t* crow, int32_t n0, int32_t ncols, int32_t N)
+{
+    for (int32_t c = 0; c < ncols; c += 8) {
+        const int32_t n = n0 + c;
+        if (n + 8 <= N) {
+            *reinterpret_cast<uint4*>(crow + n) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            for (int32_t e = 0; e < 8 && n + e < N; ++e) crow[n + e] = 0;
+        }
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_half2_rn(uint32_t lo_bits, uint32_t hi_bits)
 {
     const __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
@@ -107,16 +122,19 @@ constexpr int kEpiWarpStagingBytes = 2 * kEpiBufBytes;
 //   t_row     tensor-memory address of (this warp's first lane, first column)
 //   staging   this warp's 2 x 2 KiB staging buffers (1024-byte aligned)
 //   c_row0    first C row of this warp's 32 rows; n0 first C column of the tile
-//   M, N      extents of C
+//   M, N, C, ldc  extents, base and row pitch of C
 //   release   called by every lane once all tensor-memory reads are done
-// The accumulator is narrowed to fp16 once (round to nearest even). Parts of
-// a 32 x 32 block outside C are clipped by the TMA unit; blocks entirely
-// outside C are not stored. Only lane 0 issues stores, so lane 0 alone waits
-// on the bulk groups.
+// The accumulator is narrowed to fp16 once (round to nearest even). Rows past
+// M are clipped by the TMA unit; blocks entirely outside C are not stored.
+// The TMA unit writes whole 16-byte granules at the right edge of the tensor,
+// so a block whose columns end inside a granule past N (N not a multiple of
+// 8) is written with masked direct stores instead, leaving C's padding
+// columns untouched. Only lane 0 issues TMA stores, so lane 0 alone waits on
+// the bulk groups.
 template <int TN, class Release>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* staging, const CUtensorMap* tmap_c,
-                                                   int32_t c_row0, int32_t n0, int32_t M, int32_t N, int lane,
-                                                   Release release)
+                                                   int32_t c_row0, int32_t n0, int32_t M, int32_t N,
+                                                   uint16_t* C, int64_t ldc, int lane, Release release)
 {
     const uint32_t stage0 = smem_addr(staging);
     const uint32_t row_off = static_cast<uint32_t>(lane) * 64u;
@@ -130,6 +148,18 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
         uint32_t h[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r[2 * i], r[2 * i + 1]);
+        const int32_t x = n0 + c * kEpiChunkCols;
+        if ((N & 7) != 0 && x + kEpiChunkCols > N) {  // right edge inside a 16-byte granule
+            const int32_t row = c_row0 + lane;
+            if (row < M && x < N) {
+                uint16_t* dst = C + static_cast<int64_t>(row) * ldc + x;
+#pragma unroll
+                for (int e = 0; e < kEpiChunkCols; ++e) {
+                    if (x + e < N) dst[e] = static_cast<uint16_t>(e & 1 ? (h[e >> 1] >> 16) : (h[e >> 1] & 0xFFFFu));
+                }
+            }
+            continue;
+        }
         const uint32_t buf = stage0 + static_cast<uint32_t>((c & 1) * kEpiBufBytes);
         if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
         __syncwarp();
@@ -140,7 +170,6 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            const int32_t x = n0 + c * kEpiChunkCols;
             if (c_row0 < M && x < N) tma_store_2d(tmap_c, staging + (c & 1) * kEpiBufBytes, x, c_row0);
             bulk_commit_group();  // an empty group keeps the per-buffer accounting uniform
         }

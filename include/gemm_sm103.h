@@ -54,8 +54,10 @@ extern "C" {
 typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = 1, /* negative extent, group_size_m <= 0, NULL with work to do, aliasing */
-    GEMM_ERR_UNSUPPORTED = 2, /* a TMA constraint: pointer not 16-byte aligned, N or K not a
-                                 multiple of 8, an extent above 2^30, an unknown tile config */
+    GEMM_ERR_UNSUPPORTED = 2, /* a TMA constraint: pointer not 16-byte aligned, a row pitch not a
+                                 multiple of 8 elements (for the contiguous entry points: N or
+                                 K not a multiple of 8), an extent above 2^30, an unknown tile
+                                 config */
     GEMM_ERR_CUDA = 3,        /* a CUDA runtime call failed (see gemm_last_cuda_error) */
     GEMM_ERR_TIMEOUT = 4      /* a kernel's bounded wait expired (reported by gemm_query_status) */
 } gemm_status_t;
@@ -106,6 +108,27 @@ int gemm_f16_f32acc(const void* A, const void* B, void* C, int64_t M, int64_t N,
  */
 int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                           int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace, void* stream);
+
+/*
+ * As gemm_f16_f32acc_tiled with explicit row pitches (leading dimensions),
+ * for operands that are views into larger row-major arrays. This covers the
+ * general strides of the Triton tutorial's pointer arithmetic (the kernl
+ * notebook's last code cell: stride_am, stride_bk, stride_cm with unit column
+ * strides):
+ *
+ *   element (i,k) of A at A + i*lda + k,  (k,j) of B at B + k*ldb + j,
+ *   element (i,j) of C at C + i*ldc + j.
+ *
+ *   lda >= K, ldb >= N, ldc >= N, each a multiple of 8 elements (16 bytes) and
+ *   at most 2^30; A, B, C 16-byte aligned. M, N, K need no alignment: loads
+ *   past the extents read zeros and stores stop at column N, so the padding
+ *   columns [N, ldc) of C are never written. Errors as for gemm_f16_f32acc
+ *   (a pitch below its row length is GEMM_ERR_INVALID_ARG, a misaligned pitch
+ *   GEMM_ERR_UNSUPPORTED). Column strides other than 1 are not supported.
+ */
+int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t M,
+                            int64_t N, int64_t K, int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace,
+                            void* stream);
 
 /*
  * Tile shape a configuration uses for a problem (GEMM_TILE_AUTO depends on M): writes TILE_M, TILE_N,

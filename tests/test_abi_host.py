@@ -99,3 +99,31 @@ def test_python_binding_rejects_host_tensors(lib):
         g.gemm(a, a)
     with pytest.raises(TypeError):
         g.gemm(a.float(), a)
+
+
+def _strided(lib, A=16, lda=64, B=16, ldb=64, C=16, ldc=64, M=64, N=64, K=64):
+    return lib.gemm_f16_f32acc_strided(A, lda, B, ldb, C, ldc, M, N, K, 8, 0, None, None)
+
+
+def test_strided_validation_without_gpu(lib):
+    inv, uns = g.GEMM_ERR_INVALID_ARG, g.GEMM_ERR_UNSUPPORTED
+    big = 1 << 40
+    assert _strided(lib, lda=56) == inv            # pitch shorter than the row
+    assert _strided(lib, ldb=63) == inv
+    assert _strided(lib, ldc=8) == inv
+    assert _strided(lib, lda=68) == uns            # pitch not a multiple of 8 elements
+    assert _strided(lib, ldc=100) == uns
+    assert _strided(lib, ldb=(1 << 30) + 8) == uns
+    assert _strided(lib, A=big, lda=1024, B=2 * big, C=big + 1024 * 2 * 63, ldc=1024) == inv  # C inside A's rows
+    assert _strided(lib, M=0, A=0, B=0, C=0) == g.GEMM_OK
+    # the contiguous entry point keeps its N % 8, K % 8 rule through the pitch rule
+    assert lib.gemm_f16_f32acc(16, 16, 16, 64, 60, 64, 8, None) == uns
+
+
+def test_python_binding_accepts_padded_rows_only(lib):
+    base = torch.zeros((8, 16), dtype=torch.float16)
+    assert g._binding._row_major(base[:, :10])            # padded rows
+    assert not g._binding._row_major(base.t())            # column-major
+    assert not g._binding._row_major(base[:, ::2])        # column stride 2
+    assert g._binding._ld(base[:, :10]) == 16
+    assert g._binding._ld(base[:1, :3]) == 8 and g._binding._ld(torch.zeros((1, 13), dtype=torch.float16)) == 16

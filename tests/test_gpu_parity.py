@@ -143,3 +143,42 @@ def test_non_default_stream_and_out(gemm_lib):
     s.synchronize()
     assert r.data_ptr() == out.data_ptr()
     check_against_oracle(A, B, out)
+
+
+STRIDED = [
+    # (M, N, K, lda, ldb, ldc): odd extents inside padded rows, and views of wider arrays
+    (300, 999, 1001, 1008, 1000, 1000),
+    (257, 264, 72, 80, 272, 264),
+    (1000, 100, 37, 64, 104, 128),
+    (4095, 3000, 1000, 1024, 3072, 3008),
+    (1, 7, 3, 8, 8, 8),
+]
+
+
+@pytest.mark.parametrize("cfg", [g.TILE_AUTO, g.TILE_128x256x64, g.TILE_256x256x64_PAIR])
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc", STRIDED)
+def test_strided_views(gemm_lib, M, N, K, lda, ldb, ldc, cfg):
+    A, B = inputs.gemm_inputs(M, N, K, seed=M + 3 * N + 7 * K)
+    a_buf = torch.full((M, lda), float("nan"), dtype=torch.float16)
+    b_buf = torch.full((K, ldb), float("nan"), dtype=torch.float16)
+    a_buf[:, :K] = A
+    b_buf[:, :N] = B
+    canary = 0x7E01
+    c_buf = torch.full((M, ldc), canary, dtype=torch.int16, device="cuda")
+    a_view = a_buf.cuda()[:, :K]
+    b_view = b_buf.cuda()[:, :N]
+    c_view = c_buf.view(torch.float16)[:, :N]
+    g.gemm(a_view, b_view, out=c_view, tile_cfg=cfg)   # the NaN padding of A and B is never read
+    assert g.query_status() == g.GEMM_OK
+    check_against_oracle(A, B, c_view.contiguous())
+    assert torch.all(c_buf[:, N:] == canary)          # padding columns of C untouched
+
+
+def test_strided_k_zero_stops_at_n(gemm_lib):
+    M, N, ldc = 300, 999, 1008
+    c_buf = torch.full((M, ldc), 0x7E01, dtype=torch.int16, device="cuda")
+    a = torch.empty((M, 0), dtype=torch.float16, device="cuda")
+    b = torch.empty((0, N), dtype=torch.float16, device="cuda")
+    g.gemm(a, b, out=c_buf.view(torch.float16)[:, :N])
+    assert g.query_status() == g.GEMM_OK
+    assert torch.all(c_buf[:, :N] == 0) and torch.all(c_buf[:, N:] == 0x7E01)
