@@ -1,6 +1,7 @@
 """Seeded synthetic inputs, shared by the tests and the benchmark.
 
-This module holds no GEMM arithmetic: it only draws operands and picks rows.
+This module holds no GEMM or softmax arithmetic: it only draws operands and
+picks rows.
 
 Recipe (the check of "03: Matrix multiplication", phobos-lang.dev tutorial,
 seeds and shapes as listed in WORKLOADS): a host generator seeded with
@@ -63,3 +64,41 @@ WORKLOADS = [
 ]
 
 WORKLOADS_BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def softmax_inputs(M: int, n: int, ld: int, seed: int, pad_value: float = 0.0) -> torch.Tensor:
+    """X [M, ld] fp32 on the host: standard normal in the first n columns, `pad_value` after.
+
+    Recipe (the check of "02: Fused softmax", phobos-lang.dev tutorial): a
+    host generator seeded with `seed`, then randn([M, n]) in fp32, stored in
+    rows `ld` wide (the tutorial stores its 781-column rows 784 wide).
+    """
+    if ld < n:
+        raise ValueError("ld must be at least n")
+    g = torch.Generator().manual_seed(seed)
+    x = torch.full((M, ld), pad_value, dtype=torch.float32)
+    x[:, :n] = torch.randn((M, n), generator=g, dtype=torch.float32)
+    return x
+
+
+@dataclass(frozen=True)
+class SoftmaxWorkload:
+    name: str
+    M: int
+    n: int
+    ld: int
+    seed: int
+    sampled: bool = False      # verified on 256 seeded rows instead of every row
+
+
+# The tutorial's 1823 x 781 input in 784-wide rows; the same row length over
+# enough rows that the arrays exceed L2 (the bandwidth measurement); wider
+# rows that one warp cannot hold (one CTA per row).
+SOFTMAX_WORKLOADS = [
+    SoftmaxWorkload("softmax_1823x781", 1823, 781, 784, 0),
+    SoftmaxWorkload("softmax_262144x781", 262144, 781, 784, 8, sampled=True),
+    SoftmaxWorkload("softmax_8192x8000", 8192, 8000, 8000, 9, sampled=True),
+    SoftmaxWorkload("softmax_4096x32768", 4096, 32768, 32768, 10, sampled=True),
+]
+
+SOFTMAX_WORKLOADS_BY_NAME = {w.name: w for w in SOFTMAX_WORKLOADS}

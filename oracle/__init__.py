@@ -11,6 +11,7 @@ Contents:
                    round-to-nearest-even narrowing to fp16
   gemm.py          ctypes front end of gemm_oracle.c
   build.py         gcc build of gemm_oracle.c
+  softmax.py       the row softmax of the fused-softmax tutorial, numpy fp64
 
 Pins (the tests that tie the oracle to something other than itself):
   tile map         the notebook's printed worked example (tests/golden/),
