@@ -21,6 +21,8 @@ the host and copied to the device before timing). Rank 0 prints one JSON line.
 * cpu_baseline: the CPU oracle on a bounded, seeded sample of rows of the
   same workload, timed on this host's cores (rank 0 only).
 * --impl reference: the oracle alone as the reference arm, on the host.
+* --workload softmax_<M>x<n>: the fused row softmax instead (GB/s of 8 bytes
+  per element, roofline against the measured HBM copy bandwidth).
 Multi-GPU (torchrun): replicas only. Every rank runs the same workload on its
 own GPU with no collective on the data path; scaling is weak.
 """
@@ -47,14 +49,20 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: identifies the kernel an ncu capture measured."""
+KERNEL_SOURCES = {
+    "gemm": ["gemm_api.cu", "gemm_kernel.cuh", "gemm_kernel_pair.cuh", "kernel_common.cuh", "ptx.cuh",
+             "tile_map.cuh"],
+    "softmax": ["softmax_api.cu", "softmax_kernel.cuh", "ptx.cuh"],
+}
+
+
+def kernel_source_hash(kind: str = "gemm") -> str:
+    """Hash of the CUDA sources of one kernel family: identifies the kernel an ncu capture measured."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp16_gemm_fp32_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES[kind]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -68,15 +76,15 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def load_traffic(workload: str, tile: str, group_size_m: int):
-    """DRAM bytes per launch recorded by ncu for this kernel source, or None."""
+def load_traffic(key: str, kind: str = "gemm"):
+    """DRAM bytes per launch recorded by ncu under `key` for this kernel source, or None."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    e = d.get(f"{workload}/{tile}/G{group_size_m}")
-    if not e or e.get("kernel_hash") != kernel_source_hash():
+    e = d.get(key)
+    if not e or e.get("kernel_hash") != kernel_source_hash(kind):
         return None
     return float(e["dram_bytes_per_launch"])
 
@@ -333,7 +341,7 @@ def run_ours(args, w, rank, world, local_rank):
         "config": config_dict(w, args, tile),
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": load_traffic(w.name, tile, args.group_size_m),
+                     "frac": achieved / peak, "traffic": load_traffic(f"{w.name}/{tile}/G{args.group_size_m}"),
                      "peak_source": f"{peak_src} dense bf16 burst (bf16_tflops, MEASURED_PEAKS.json); "
                                     "fp16 and bf16 share the tensor rate",
                      "kernel": f"{kernel_name} {tile}", "kernel_ms": kernel_ms,
@@ -351,64 +359,223 @@ def run_ours(args, w, rank, world, local_rank):
     return 0
 
 
-def run_e2e(args, w, g, A, B, dev, world):
-    """Steps of host A, B -> device -> GEMM -> host C, all through the public
+def pipelined_e2e(steps, dev, world, host_in, out_like, fn, label):
+    """Steps of host inputs -> device -> fn -> host output, through the public
     API. Every step copies its own inputs in and its result out; copies of
-    step i+1 and i-1 overlap the GEMM of step i (separate H2D, compute and D2H
-    streams, double-buffered device operands). Returns (ms, steps, mode)."""
+    step i+1 and i-1 overlap the compute of step i (separate H2D, compute and
+    D2H streams, double-buffered device buffers). Returns (ms, steps, mode)."""
     import torch
-    import torch.distributed as dist
 
-    steps = max(1, min(args.steps, args.e2e_steps))
-    hA, hB = A.pin_memory(), B.pin_memory()
+    hin = [t.pin_memory() for t in host_in]
     nbuf = 2
-    dA = [torch.empty((w.M, w.K), dtype=torch.float16, device=dev) for _ in range(nbuf)]
-    dB = [torch.empty((w.K, w.N), dtype=torch.float16, device=dev) for _ in range(nbuf)]
-    dC = [torch.empty((w.M, w.N), dtype=torch.float16, device=dev) for _ in range(nbuf)]
-    hC = [torch.empty((w.M, w.N), dtype=torch.float16).pin_memory() for _ in range(nbuf)]
-    s_in, s_gemm, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev = lambda: torch.cuda.Event()  # noqa: E731
-    gemm_done = [None] * nbuf
+    din = [[torch.empty_like(t, device=dev) for t in hin] for _ in range(nbuf)]
+    dout = [torch.empty_like(out_like, device=dev) for _ in range(nbuf)]
+    hout = [torch.empty_like(out_like, device="cpu").pin_memory() for _ in range(nbuf)]
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    comp_done = [None] * nbuf
     out_done = [None] * nbuf
 
     def step(i):
         k = i % nbuf
         with torch.cuda.stream(s_in):
-            if gemm_done[k] is not None:
-                s_in.wait_event(gemm_done[k])  # the GEMM that last read dA[k], dB[k]
-            dA[k].copy_(hA, non_blocking=True)
-            dB[k].copy_(hB, non_blocking=True)
-            in_done = ev()
+            if comp_done[k] is not None:
+                s_in.wait_event(comp_done[k])  # the compute that last read din[k]
+            for d, h in zip(din[k], hin):
+                d.copy_(h, non_blocking=True)
+            in_done = torch.cuda.Event()
             in_done.record(s_in)
-        with torch.cuda.stream(s_gemm):
-            s_gemm.wait_event(in_done)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(in_done)
             if out_done[k] is not None:
-                s_gemm.wait_event(out_done[k])  # the copy that last read dC[k]
-            g.gemm(dA[k], dB[k], group_size_m=args.group_size_m, out=dC[k], tile_cfg=args.tile_cfg)
-            gemm_done[k] = ev()
-            gemm_done[k].record(s_gemm)
+                s_comp.wait_event(out_done[k])  # the copy that last read dout[k]
+            fn(din[k], dout[k])
+            comp_done[k] = torch.cuda.Event()
+            comp_done[k].record(s_comp)
         with torch.cuda.stream(s_out):
-            s_out.wait_event(gemm_done[k])
-            hC[k].copy_(dC[k], non_blocking=True)
-            out_done[k] = ev()
+            s_out.wait_event(comp_done[k])
+            hout[k].copy_(dout[k], non_blocking=True)
+            out_done[k] = torch.cuda.Event()
             out_done[k].record(s_out)
 
     for i in range(2):
         step(i)
     torch.cuda.synchronize(dev)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
-    s_gemm.wait_event(e0)
+    s_comp.wait_event(e0)
     s_out.wait_event(e0)
     for i in range(steps):
         step(i)
     s_out.wait_stream(s_in)
-    s_out.wait_stream(s_gemm)
+    s_out.wait_stream(s_comp)
     e1.record(s_out)
     torch.cuda.synchronize(dev)
-    return max_over_ranks(e0.elapsed_time(e1), dev, world), steps, "pipelined: H2D, GEMM and D2H streams, 2 buffers"
+    return max_over_ranks(e0.elapsed_time(e1), dev, world), steps, f"pipelined: H2D, {label} and D2H streams, 2 buffers"
+
+
+def run_e2e(args, w, g, A, B, dev, world):
+    import torch
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    out_like = torch.empty((w.M, w.N), dtype=torch.float16)
+    return pipelined_e2e(steps, dev, world, [A, B], out_like,
+                         lambda ins, out: g.gemm(ins[0], ins[1], group_size_m=args.group_size_m, out=out,
+                                                 tile_cfg=args.tile_cfg), "GEMM")
+
+
+# ---------------------------------------------------------------- softmax workloads
+SOFTMAX_METRIC = "fp32 row softmax GB/s (8 bytes per element: x read, y written)"
+
+
+def softmax_config(w, args):
+    mib = (4 * w.M * w.ld) >> 20
+    return {"workload": w.name, "M": w.M, "n": w.n, "ld": w.ld, "seed": w.seed,
+            "inputs": "x = torch.randn(fp32, host generator seeded) in rows ld wide",
+            "l2": ("flush: a 256 MiB buffer is written between timed steps" if args.flush_l2 else
+                   f"x and y are {mib} MiB each vs 129 MB L2" + ("" if 2 * mib > 129 else " (L2-resident)")),
+            "parallelism": "replicas"}
+
+
+def time_softmax_oracle(x, n, rows):
+    from oracle import softmax as osm
+    t = time.perf_counter()
+    osm.softmax_rows(x, n, rows=rows)
+    return time.perf_counter() - t
+
+
+def softmax_cpu_baseline(x, w, target_s):
+    """The numpy fp64 oracle on a seeded sample of rows: ~target_s of work."""
+    import numpy as np
+    import torch
+    g = torch.Generator().manual_seed(w.seed + 2000)
+    perm = torch.randperm(w.M, generator=g).numpy()
+    calib = min(w.M, 64)
+    per_row = max(time_softmax_oracle(x, w.n, np.sort(perm[:calib])) / calib, 1e-7)
+    k = int(min(w.M, max(calib, target_s / per_row)))
+    rows = np.sort(perm[:k])
+    t = time_softmax_oracle(x, w.n, rows)
+    return {"value": 8.0 * k * w.n / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{k} seeded rows of the {w.M}x{w.n} workload, {t:.1f} s, numpy fp64 max/exp/sum/divide"}
+
+
+def run_softmax_reference(args, w, rank, world):
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+    from dense_fp16_gemm_fp32_gb300 import inputs
+
+    x = inputs.softmax_inputs(w.M, w.n, w.ld, w.seed).numpy()
+    g = torch.Generator().manual_seed(w.seed + 3000)
+    perm = torch.randperm(w.M, generator=g).numpy()
+    calib = min(w.M, 64)
+    per_row = max(time_softmax_oracle(x, w.n, np.sort(perm[:calib])) / calib, 1e-7)
+    k = int(max(1, min(w.M, args.reference_budget_s / max(1, args.steps + args.warmup) / per_row)))
+    for _ in range(args.warmup):
+        time_softmax_oracle(x, w.n, np.sort(perm[:k]))
+    t = 0.0
+    for i in range(args.steps):
+        off = (i * k) % max(1, w.M - k + 1)
+        t += time_softmax_oracle(x, w.n, np.sort(perm[off:off + k]))
+    value = 8.0 * k * w.n * args.steps / t / 1e9
+    line = {
+        "impl": "reference", "metric": SOFTMAX_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": softmax_config(w, args),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{k} seeded rows of {w.M}x{w.n} per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_softmax(args, w, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import dense_fp16_gemm_fp32_gb300 as g
+    from dense_fp16_gemm_fp32_gb300 import inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    g.load()
+    X = inputs.softmax_inputs(w.M, w.n, w.ld, w.seed)
+    xp = X.to(dev)
+    yp = torch.empty_like(xp)
+    x, y = xp[:, :w.n], yp[:, :w.n]
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
+    plan = g.softmax_plan(w.M, w.n, dev)
+
+    for _ in range(args.warmup):
+        g.softmax(x, out=y)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0).start() if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    n_launch0 = g.softmax_launch_count()
+    t_host0 = time.time()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        g.softmax(x, out=y)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    if world > 1:
+        dist.barrier()
+    launches = g.softmax_launch_count() - n_launch0
+    if sampler is not None:
+        sampler.stop()
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(per_launch_ms) if args.flush_l2 else starts[0].elapsed_time(ends[-1])
+    total_ms_max = max_over_ranks(total_ms, dev, world)
+
+    steps_e2e = max(1, min(args.steps, args.e2e_steps))
+    e2e_ms, e2e_steps, e2e_mode = pipelined_e2e(
+        steps_e2e, dev, world, [X], X, lambda ins, out: g.softmax(ins[0][:, :w.n], out=out[:, :w.n]), "softmax")
+
+    if rank != 0:
+        return 0
+    nbytes = 8.0 * w.M * w.n   # algorithmic: each element read once and written once
+    value = nbytes * args.steps * world / (total_ms_max * 1e-3) / 1e9
+    kernel_ms = statistics.fmean(per_launch_ms)
+    achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    kind = ("softmax_rows_warp_kernel" if plan["threads_per_row"] == 32 else
+            "softmax_rows_cta_kernel" + (f" cluster {plan['cluster_ctas']}" if plan["cluster_ctas"] > 1 else ""))
+    line = {
+        "metric": SOFTMAX_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": softmax_config(w, args),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": load_traffic(f"{w.name}/softmax", "softmax"),
+                     "peak_source": f"{peak_src} HBM copy bandwidth (hbm_gbs, MEASURED_PEAKS.json)",
+                     "kernel": kind, "kernel_ms": kernel_ms, "bytes_per_launch": nbytes, "plan": plan},
+        "e2e": {"value": 8.0 * w.M * w.n * e2e_steps * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": X.numel() * 4, "d2h_bytes_per_step": X.numel() * 4,
+                "steps": e2e_steps, "mode": e2e_mode},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(t_host0, t_host1) if sampler is not None else None,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = softmax_cpu_baseline(X.numpy(), w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def main():
@@ -430,19 +597,28 @@ def main():
         p.error("--warmup must be >= 3")
 
     from dense_fp16_gemm_fp32_gb300 import inputs
-    w = inputs.WORKLOADS_BY_NAME[args.workload]
+    softmax = args.workload in inputs.SOFTMAX_WORKLOADS_BY_NAME
+    if softmax:
+        w = inputs.SOFTMAX_WORKLOADS_BY_NAME[args.workload]
+    elif args.workload in inputs.WORKLOADS_BY_NAME:
+        w = inputs.WORKLOADS_BY_NAME[args.workload]
+    else:
+        p.error(f"unknown workload {args.workload}; one of "
+                + ", ".join(list(inputs.WORKLOADS_BY_NAME) + list(inputs.SOFTMAX_WORKLOADS_BY_NAME)))
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
-        return run_reference(args, w, rank, world)
+        return run_softmax_reference(args, w, rank, world) if softmax else run_reference(args, w, rank, world)
     if world > 1:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
+        if softmax:
+            return run_softmax(args, w, rank, world, local_rank)
         return run_ours(args, w, rank, world, local_rank)
     finally:
         if world > 1:

@@ -1,10 +1,12 @@
-"""fp16 GEMM with fp32 accumulation for GB300 (sm_103a).
+"""fp16 GEMM with fp32 accumulation for GB300 (sm_103a), and a fused row softmax.
 
     C[M,N] = A[M,K] @ B[K,N]   (fp16 in, fp32 accumulate, fp16 out, rounded once)
+    Y[i,:] = softmax(X[i,:n])  (fp32, one pass over memory)
 
-The work runs in hand-written tcgen05/TMA kernels behind a C ABI
-(include/gemm_sm103.h, libgemm_sm103.so); this package is its thin Python
-binding plus the seeded synthetic inputs used by the tests and the benchmark.
+The work runs in hand-written CUDA kernels (tcgen05/TMA for the GEMM) behind
+a C ABI (include/gemm_sm103.h, include/softmax_sm103.h, libgemm_sm103.so);
+this package is its thin Python binding plus the seeded synthetic inputs
+used by the tests and the benchmark.
 """
 from ._binding import (  # noqa: F401
     DEFAULT_GROUP_SIZE_M,
@@ -13,6 +15,7 @@ from ._binding import (  # noqa: F401
     GEMM_ERR_TIMEOUT,
     GEMM_ERR_UNSUPPORTED,
     GEMM_OK,
+    SOFTMAX_MAX_COLS,
     TILE_128x64x32,
     TILE_128x256x64,
     TILE_256x256x64_PAIR,
@@ -29,6 +32,9 @@ from ._binding import (  # noqa: F401
     query_status,
     set_fault_injection,
     set_watchdog_ns,
+    softmax,
+    softmax_launch_count,
+    softmax_plan,
     status_string,
     tile_schedule,
     tile_shape,

@@ -30,6 +30,7 @@ TILE_256x256x128_PAIR = 4
 DEFAULT_GROUP_SIZE_M = 8
 
 HEADER = os.path.join(_build.ROOT, "include", "gemm_sm103.h")
+HEADERS = [HEADER, os.path.join(_build.ROOT, "include", "softmax_sm103.h")]
 
 
 class GemmError(RuntimeError):
@@ -64,7 +65,13 @@ _SIGNATURES = {
     "gemm_launch_count": (ctypes.c_uint64, []),
     "gemm_f16_f32acc_noalloc": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, ctypes.c_int64, ctypes.c_int64,
                                                ctypes.c_int64, ctypes.c_int32, _c_void_p, _c_void_p]),
+    "softmax_rows_f32": (ctypes.c_int, [_c_void_p, ctypes.c_int64, _c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_int64, _c_void_p]),
+    "softmax_rows_plan": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, _c_void_p, _c_void_p, _c_void_p]),
+    "softmax_launch_count": (ctypes.c_uint64, []),
 }
+
+SOFTMAX_MAX_COLS = 65536
 
 
 def lib_path() -> str:
@@ -90,11 +97,14 @@ def load():
 
 
 def header_functions() -> list[str]:
-    """Names of the functions include/gemm_sm103.h declares."""
-    with open(HEADER) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gemm_\w+)\s*\(", text, flags=re.M)
+    """Names of the functions include/gemm_sm103.h and include/softmax_sm103.h declare."""
+    names = []
+    for path in HEADERS:
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:gemm|softmax)_\w+)\s*\(", text, flags=re.M)
+    return names
 
 
 def status_string(code: int) -> str:
@@ -236,3 +246,66 @@ def launch_count() -> int:
 
 def last_cuda_error() -> int:
     return int(load().gemm_last_cuda_error())
+
+
+def _check_rows(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device, got {t.device}")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(t.shape)}")
+    if not _row_major(t):
+        raise ValueError(f"{name} must be row-major: unit column stride and a row stride >= its columns")
+
+
+def _row_pitch(t: torch.Tensor) -> int:
+    """Row pitch in elements; a one-row tensor's pitch addresses nothing and
+    is reported as its row length rounded up to 4."""
+    if t.shape[0] > 1:
+        return int(t.stride(0))
+    return max(4, -(-int(t.shape[1]) // 4) * 4)
+
+
+def softmax(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Row softmax of x along dim 1 (fp32), as the fused-softmax tutorial computes it.
+
+    x: [M, n] fp32 CUDA, row-major; a view with padded rows (stride (ld, 1),
+    ld >= n) is read in place and its padding is not read.
+    out: optional [M, n] fp32 CUDA row-major tensor or padded view (may be x
+    itself); its padding columns are not written. By default the result is a
+    [M, n] view of a new array whose rows are padded to a multiple of 4
+    elements, so that every row starts on a 16-byte boundary.
+    Runs on the current CUDA stream of x's device.
+    """
+    _check_rows(x, "x")
+    M, n = x.shape
+    if out is None:
+        ld = max(4, -(-n // 4) * 4)
+        out = torch.empty((M, ld), dtype=torch.float32, device=x.device)[:, :n]
+    else:
+        _check_rows(out, "out")
+        if tuple(out.shape) != (M, n) or out.device != x.device:
+            raise ValueError(f"out must be [{M},{n}] on {x.device}")
+    lib = load()
+    with torch.cuda.device(x.device):
+        rc = lib.softmax_rows_f32(x.data_ptr(), _row_pitch(x), out.data_ptr(), _row_pitch(out), M, n,
+                                  _stream_ptr(x.device))
+    _check(rc, "softmax_rows_f32")
+    return out
+
+
+def softmax_plan(M: int, n: int, device=None) -> dict:
+    """The launch softmax() makes for M rows of n columns: threads and CTAs per row, grid CTAs."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    tpr, cl, grid = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    with torch.cuda.device(device):
+        rc = load().softmax_rows_plan(M, n, ctypes.byref(tpr), ctypes.byref(cl), ctypes.byref(grid))
+    _check(rc, "softmax_rows_plan")
+    return {"threads_per_row": tpr.value, "cluster_ctas": cl.value, "grid_ctas": grid.value}
+
+
+def softmax_launch_count() -> int:
+    return int(load().softmax_launch_count())

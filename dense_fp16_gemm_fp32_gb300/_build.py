@@ -1,8 +1,10 @@
 """Builds the CUDA library ``libgemm_sm103.so`` in-tree with nvcc (sm_103a only).
 
-One translation unit (csrc/gemm_api.cu, which includes the kernels), one
--gencode, so a build takes seconds. The shared cudart is used so the library
-and PyTorch share one CUDA runtime in the process.
+One translation unit per API file (csrc/gemm_api.cu with the GEMM kernels,
+csrc/softmax_api.cu with the softmax kernels), compiled in parallel with one
+-gencode each and linked into one shared library, so a build takes seconds.
+The shared cudart is used so the library and PyTorch share one CUDA runtime
+in the process.
 """
 from __future__ import annotations
 
@@ -18,6 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgemm_sm103.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+UNITS = ["gemm_api.cu", "softmax_api.cu"]
 
 
 def _nvcc() -> str:
@@ -48,13 +51,31 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     if not force and not stale():
         return LIB
     nvcc = _nvcc()
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-cudart", "shared", f"-I{INCLUDE}", "-Xlinker", f"-rpath,{_cuda_lib_dir(nvcc)}",
-           *(extra_flags or []), "-o", tmp, os.path.join(CSRC, "gemm_api.cu")]
-    if verbose:
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
+    tag = f".tmp{os.getpid()}"
+    tmp = LIB + tag
+    compile_flags = [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}",
+                     *(extra_flags or [])]
+    objs, procs = [], []
+    for unit in UNITS:
+        obj = os.path.join(PKG, f"{os.path.splitext(unit)[0]}.{os.getpid()}.o")
+        cmd = [nvcc, *compile_flags, "-c", "-o", obj, os.path.join(CSRC, unit)]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        objs.append(obj)
+        procs.append(subprocess.Popen(cmd))
+    try:
+        failed = [p.args[-1] for p in procs if p.wait() != 0]
+        if failed:
+            raise subprocess.CalledProcessError(1, f"nvcc {' '.join(failed)}")
+        cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", f"-rpath,{_cuda_lib_dir(nvcc)}",
+               "-o", tmp, *objs]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        subprocess.run(cmd, check=True)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     os.replace(tmp, LIB)
     return LIB
 

@@ -365,6 +365,12 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
 
 }  // namespace
 
+namespace gemm103 {
+// Shared with the other translation units of the library (softmax_api.cu):
+// records a failed CUDA call for gemm_last_cuda_error.
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+}  // namespace gemm103
+
 // ---------------------------------------------------------------- no-alloc variant
 // Scratch for gemm_f16_f32acc_noalloc. Some callers may not allocate device
 // memory at the moment they run a GEMM: code being captured into a CUDA graph

@@ -216,6 +216,14 @@ __device__ __forceinline__ void cluster_wait()
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// 32-bit load from shared memory of any CTA of the cluster (a mapa address).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {

@@ -18,6 +18,7 @@ def lib():
 def test_header_declares_expected_entry_points():
     names = g.header_functions()
     for want in ("gemm_f16_f32acc", "gemm_f16_f32acc_tiled", "gemm_tile_schedule", "gemm_query_status",
+                 "softmax_rows_f32", "softmax_rows_plan", "softmax_launch_count",
                  "gemm_status_string", "gemm_tile_shape", "gemm_set_watchdog_ns", "gemm_set_fault_injection",
                  "gemm_launch_count", "gemm_last_cuda_error"):
         assert want in names
@@ -127,3 +128,49 @@ def test_python_binding_accepts_padded_rows_only(lib):
     assert not g._binding._row_major(base[:, ::2])        # column stride 2
     assert g._binding._ld(base[:, :10]) == 16
     assert g._binding._ld(base[:1, :3]) == 8 and g._binding._ld(torch.zeros((1, 13), dtype=torch.float16)) == 16
+
+
+def _softmax(lib, X=16, ldx=64, Y=1 << 40, ldy=64, M=8, n=64):
+    return lib.softmax_rows_f32(X, ldx, Y, ldy, M, n, None)
+
+
+def test_softmax_validation_without_gpu(lib):
+    inv, uns = g.GEMM_ERR_INVALID_ARG, g.GEMM_ERR_UNSUPPORTED
+    big = 1 << 40
+    assert _softmax(lib, M=-1) == inv
+    assert _softmax(lib, n=-1) == inv
+    assert _softmax(lib, ldx=63) == inv                  # pitch shorter than the row
+    assert _softmax(lib, ldy=10) == inv
+    assert _softmax(lib, X=0) == inv
+    assert _softmax(lib, Y=0) == inv
+    assert _softmax(lib, n=65537, ldx=70000, ldy=70000) == uns
+    assert _softmax(lib, ldx=(1 << 31) + 4) == uns
+    assert _softmax(lib, X=18) == uns                    # not 4-byte aligned
+    assert _softmax(lib, Y=big + 2) == uns
+    # overlapping ranges other than exact in-place
+    assert _softmax(lib, X=big, Y=big + 4 * 64 * 7) == inv
+    assert _softmax(lib, X=big, Y=big, ldx=64, ldy=128) == inv
+    # no work: OK, NULL pointers allowed
+    assert _softmax(lib, X=0, Y=0, M=0) == g.GEMM_OK
+    assert _softmax(lib, X=0, Y=0, n=0) == g.GEMM_OK
+
+
+def test_softmax_plan_shapes_without_gpu(lib):
+    tpr, cl = ctypes.c_int32(), ctypes.c_int32()
+    want = {1: (32, 1), 128: (32, 1), 1024: (32, 1), 1025: (64, 1), 4096: (128, 1), 8192: (256, 1),
+            8193: (256, 2), 16384: (256, 2), 16385: (256, 4), 32768: (256, 4), 32769: (256, 8), 65536: (256, 8)}
+    for n, shape in want.items():
+        assert lib.softmax_rows_plan(10, n, ctypes.byref(tpr), ctypes.byref(cl), None) == g.GEMM_OK
+        assert (tpr.value, cl.value) == shape, n
+    assert lib.softmax_rows_plan(10, 0, None, None, None) == g.GEMM_ERR_INVALID_ARG
+    assert lib.softmax_rows_plan(-1, 8, None, None, None) == g.GEMM_ERR_INVALID_ARG
+    assert lib.softmax_rows_plan(10, 65537, None, None, None) == g.GEMM_ERR_UNSUPPORTED
+
+
+def test_python_softmax_rejects_bad_tensors(lib):
+    with pytest.raises(ValueError):
+        g.softmax(torch.zeros((4, 8)))                   # host tensor
+    with pytest.raises(TypeError):
+        g.softmax(torch.zeros((4, 8), dtype=torch.float16))
+    assert g._binding._row_pitch(torch.zeros((1, 5))) == 8
+    assert g._binding._row_pitch(torch.zeros((3, 16))[:, :5]) == 16
