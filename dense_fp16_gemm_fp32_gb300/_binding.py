@@ -159,7 +159,8 @@ def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZ
 
     a: [M,K] fp16 CUDA row-major; b: [K,N] fp16 CUDA row-major, same device.
     Row-major views with padded rows (stride (ld, 1), ld >= columns) are
-    accepted; row pitches must then be multiples of 8 elements.
+    accepted with any pitch: pitches that are multiples of 8 elements with
+    16-byte aligned data run the TMA kernels, others a plain-load kernel.
     out: optional [M,N] fp16 CUDA row-major tensor (or padded view) to write;
     its padding columns are not touched.
     trace: optional int32 CUDA tensor of 3 * num_tiles entries that receives

@@ -20,6 +20,8 @@ using namespace gemm103;
 
 using Cfg128x256 = TileCfg<128, 256, 64, 4>;
 using Cfg128x64 = TileCfg<128, 64, 32, 6>;
+using CfgGeneric = TileCfg<128, 256, 64, 4, true>;  // plain loads and stores (operands TMA cannot address)
+constexpr int kGenericCfgId = 5;
 using CfgPair256 = PairCfg<6>;
 using CfgPair256Deep = PairCfg<3, 128>;
 
@@ -28,7 +30,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumCfgs = 5;
+constexpr int kNumCfgs = 6;  // the five tile configurations and the generic-load kernel
 constexpr int64_t kMaxExtent = int64_t(1) << 30;
 constexpr uint64_t kDefaultWatchdogNs = 2000000000ull;
 
@@ -144,10 +146,8 @@ int validate(const Problem& pr)
     if (pr.ldc > kMaxExtent || pr.lda > kMaxExtent || pr.ldb > kMaxExtent) return GEMM_ERR_UNSUPPORTED;
     const uintptr_t a = reinterpret_cast<uintptr_t>(pr.A), b = reinterpret_cast<uintptr_t>(pr.B),
                     c = reinterpret_cast<uintptr_t>(pr.C);
-    // TMA: 16-byte aligned bases and row pitches that are multiples of 16 bytes
-    if ((c & 15u) != 0 || (pr.ldc & 7) != 0) return GEMM_ERR_UNSUPPORTED;
-    if (pr.K > 0 && ((a & 15u) != 0 || (b & 15u) != 0 || (pr.lda & 7) != 0 || (pr.ldb & 7) != 0))
-        return GEMM_ERR_UNSUPPORTED;
+    // fp16 elements: 2-byte aligned bases
+    if ((c & 1u) != 0 || (pr.K > 0 && ((a & 1u) != 0 || (b & 1u) != 0))) return GEMM_ERR_UNSUPPORTED;
     // C must not overlap A or B (byte ranges spanned by the pitched rows)
     using u128 = unsigned __int128;
     const u128 c_end = static_cast<u128>(c) + (static_cast<u128>(pr.M - 1) * pr.ldc + pr.N) * 2;
@@ -158,6 +158,18 @@ int validate(const Problem& pr)
         if (c < b_end && b < c_end) return GEMM_ERR_INVALID_ARG;
     }
     return GEMM_OK;
+}
+
+// Tensor maps can describe the operands: 16-byte aligned bases and row
+// pitches that are multiples of 16 bytes (8 elements). Otherwise the
+// generic-load kernel runs.
+bool tma_ok(const Problem& pr)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(pr.A), b = reinterpret_cast<uintptr_t>(pr.B),
+                    c = reinterpret_cast<uintptr_t>(pr.C);
+    if ((c & 15u) != 0 || (pr.ldc & 7) != 0) return false;
+    if (pr.K > 0 && ((a & 15u) != 0 || (b & 15u) != 0 || (pr.lda & 7) != 0 || (pr.ldb & 7) != 0)) return false;
+    return true;
 }
 
 // GEMM_TILE_AUTO: the CTA-pair 256x256 tile with 128-deep k steps unless the
@@ -213,10 +225,11 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     CUtensorMap ma, mb, mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
+    std::memset(&mc, 0, sizeof(mc));
     // C: 32 x 32 store boxes, 64-byte swizzle (matches the epilogue staging layout)
-    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!Cfg::kGeneric) rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc != GEMM_OK) return rc;
-    if (pr.K > 0) {
+    if (pr.K > 0 && !Cfg::kGeneric) {
         const CUtensorMapSwizzle a_swz = Cfg::TK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
         rc = make_map(&ma, pr.A, pr.K, pr.M, pr.lda, Cfg::TK, Cfg::TM, a_swz);
         if (rc != GEMM_OK) return rc;
@@ -241,6 +254,10 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     p.fault_mode = g_fault_mode.load();
     p.num_full_tiles = p.num_tiles;
     p.num_units = p.num_tiles;
+    p.A = static_cast<const uint16_t*>(pr.A);
+    p.B = static_cast<const uint16_t*>(pr.B);
+    p.lda = pr.lda;
+    p.ldb = pr.ldb;
 
     const int64_t slots = static_cast<int64_t>(d->sm_count) * d->ctas_per_sm[cfg_id];
     const unsigned grid = static_cast<unsigned>(num_tiles < slots ? num_tiles : slots);
@@ -345,6 +362,8 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     p.trace = trace;
     p.watchdog_ns = watchdog_ns();
     p.fault_mode = g_fault_mode.load();
+    p.A = p.B = nullptr;  // the pair kernel loads through its tensor maps
+    p.lda = p.ldb = 0;
 
     const int64_t split = split_tail_tiles(num_tiles, slots);
     p.num_full_tiles = static_cast<int32_t>(num_tiles - split);
@@ -444,6 +463,7 @@ int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t l
     int rc = validate(pr);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!tma_ok(pr)) return launch<CfgGeneric>(pr, kGenericCfgId, tile_trace, s);
     switch (cfg) {
         case GEMM_TILE_128x64x32:
             return launch<Cfg128x64>(pr, cfg, tile_trace, s);
@@ -589,6 +609,7 @@ int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, in
     const Problem pr{A, B, C, M, N, K, group_size_m, K, N, N};
     int rc = validate(pr);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    if (!tma_ok(pr)) return GEMM_ERR_UNSUPPORTED;  // tensor-map operands only
     if (noalloc_scratch_words_needed() > kNoAllocScratchWords) return GEMM_ERR_UNSUPPORTED;
     NoAllocDeviceState* d = nullptr;
     rc = noalloc_setup(&d);
@@ -629,6 +650,8 @@ int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, in
     p.fault_mode = 0;
     p.num_full_tiles = p.num_tiles;
     p.num_units = p.num_tiles;
+    p.A = p.B = nullptr;
+    p.lda = p.ldb = 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The scratch keeps the previous call's contents: the status word starts at zero.

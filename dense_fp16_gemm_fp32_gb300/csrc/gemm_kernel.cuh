@@ -10,7 +10,8 @@
 // visited in the grouped order of the kernl notebook "2 - matmul offsets.ipynb"
 // (tile_map.cuh).
 //
-// GB300 mapping (one CTA of 192 threads per SM, persistent over tiles):
+// GB300 mapping (one CTA of 192 threads per SM, persistent over tiles; the
+// generic-load form adds loader warps 6..8, see TileCfg):
 //   warp 0           TMA producer (lane 0 issues): per k step, one A box (TILE_K x TILE_M,
 //                    K contiguous) and TILE_N/64 B boxes (64 x TILE_K, N
 //                    contiguous) into an S-stage shared-memory ring, tracked by
@@ -45,14 +46,20 @@
 
 namespace gemm103 {
 
-template <int TM_, int TN_, int TK_, int STAGES_>
+// kGeneric: the stages are filled by plain loads (load_stage_generic) from
+// warps 0, 6, 7 and 8 instead of TMA, and C is written with direct stores,
+// for operands whose base or row pitch a tensor map cannot describe.
+template <int TM_, int TN_, int TK_, int STAGES_, bool kGeneric_ = false>
 struct TileCfg {
     static constexpr int TM = TM_, TN = TN_, TK = TK_, STAGES = STAGES_;
+    static constexpr bool kGeneric = kGeneric_;
     static_assert(TM == 128, "one-CTA tcgen05 tile: 128 accumulator lanes");
     static_assert(TN % 64 == 0 && TN >= 64 && TN <= 256, "B is loaded in 64-column boxes; MMA N <= 256");
     static_assert(TK == 64 || TK == 32, "A rows of 128 B (128B swizzle) or 64 B (64B swizzle)");
+    static_assert(!kGeneric || TK == 64, "generic loads write the 128-byte swizzle");
 
-    static constexpr int NUM_THREADS = 192;
+    static constexpr int NUM_THREADS = kGeneric ? 192 + 96 : 192;
+    static constexpr int FULL_ARRIVALS = kGeneric ? kLoaderThreads : 1;
     static constexpr int EPI_THREADS = 128;
 
     static constexpr int A_STAGE = TM * TK * 2;      // bytes of one A panel
@@ -106,7 +113,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], Cfg::FULL_ARRIVALS);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -116,7 +123,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         mbar_init(drain, 1);
         *abort_flag = 0u;
         fence_mbar_init();
-        if (p.num_k_tiles > 0) {
+        if (p.num_k_tiles > 0 && !Cfg::kGeneric) {
             tma_prefetch_desc(&tmap_a);
             tma_prefetch_desc(&tmap_b);
             tma_prefetch_desc(&tmap_c);
@@ -132,7 +139,34 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const Watch w{abort_flag, p.status, p.watchdog_ns};
 
-    if (warp == 0) {
+    if (Cfg::kGeneric && (warp == 0 || warp >= 6)) {
+        // ------------------------------------------------------------ generic loaders
+        // Four warps fill each stage with plain loads; every thread arrives on
+        // the stage's full barrier after its writes (kLoaderThreads arrivals).
+        const int lt = (warp == 0 ? 0 : warp - 5) * 32 + lane;
+        if (p.num_k_tiles > 0 && p.fault_mode != 1) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            const uint32_t a_base = smem_addr(sA);
+            const uint32_t b_base = smem_addr(sB);
+            for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
+                for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
+                    ok = warp_wait_phase(&empty[stage], phase ^ 1u, w, kWhereProducer);
+                    if (!ok) break;
+                    load_stage_generic<Cfg::TM, Cfg::TN>(p, a_base + stage * Cfg::A_STAGE, b_base + stage * Cfg::B_STAGE,
+                                                         tc.pid_m * Cfg::TM, tc.pid_n * Cfg::TN, kt * Cfg::TK, lt);
+                    fence_proxy_async_smem();  // the tensor cores read these writes
+                    mbar_arrive(&full[stage]);
+                    if (++stage == Cfg::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------------------ producer
         // The whole warp runs the schedule; lane 0 issues.
         if (p.num_k_tiles > 0 && p.fault_mode != 1) {
@@ -253,7 +287,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::TN);
             uint64_t* release_bar = &acc_empty[buf];
-            epilogue_tma_store<Cfg::TN>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c,
+            epilogue_tma_store<Cfg::TN, Cfg::kGeneric>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c,
                                         tc.pid_m * Cfg::TM + q * 32, n0, p.M, p.N, p.C, p.ldc, lane, [&]() {
                                             tc_fence_before_sync();
                                             __syncwarp();

@@ -29,6 +29,11 @@ struct GemmParams {
     // column halves each; work units are the full tiles followed by the halves.
     int32_t num_full_tiles;
     int32_t num_units;
+    // Generic-load kernel only (operands TMA cannot describe): A and B through
+    // plain loads, row pitches in elements, any value >= the row length.
+    const uint16_t* A;
+    const uint16_t* B;
+    int64_t lda, ldb;
 };
 
 struct Watch {
@@ -91,12 +96,12 @@ __device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, 
 }
 
 // C[row, n0 .. n0 + ncols) = +0 for the columns below N (the K == 0 case).
-// crow + n0 is 16-byte aligned; no element at or past column N is written.
+// No element at or past column N is written.
 __device__ __forceinline__ void store_zero_row(uint16_t* crow, int32_t n0, int32_t ncols, int32_t N)
 {
     for (int32_t c = 0; c < ncols; c += 8) {
         const int32_t n = n0 + c;
-        if (n + 8 <= N) {
+        if (n + 8 <= N && (reinterpret_cast<uintptr_t>(crow + n) & 15u) == 0) {
             *reinterpret_cast<uint4*>(crow + n) = make_uint4(0u, 0u, 0u, 0u);
         } else {
             for (int32_t e = 0; e < 8 && n + e < N; ++e) crow[n + e] = 0;
@@ -130,8 +135,9 @@ constexpr int kEpiWarpStagingBytes = 2 * kEpiBufBytes;
 // so a block whose columns end inside a granule past N (N not a multiple of
 // 8) is written with masked direct stores instead, leaving C's padding
 // columns untouched. Only lane 0 issues TMA stores, so lane 0 alone waits on
-// the bulk groups.
-template <int TN, class Release>
+// the bulk groups. kDirect: every block is written with direct stores (C's
+// base or pitch is not one a TMA store can address).
+template <int TN, bool kDirect = false, class Release>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* staging, const CUtensorMap* tmap_c,
                                                    int32_t c_row0, int32_t n0, int32_t M, int32_t N,
                                                    uint16_t* C, int64_t ldc, int lane, Release release)
@@ -149,7 +155,7 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
 #pragma unroll
         for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r[2 * i], r[2 * i + 1]);
         const int32_t x = n0 + c * kEpiChunkCols;
-        if ((N & 7) != 0 && x + kEpiChunkCols > N) {  // right edge inside a 16-byte granule
+        if (kDirect || ((N & 7) != 0 && x + kEpiChunkCols > N)) {  // right edge inside a 16-byte granule
             const int32_t row = c_row0 + lane;
             if (row < M && x < N) {
                 uint16_t* dst = C + static_cast<int64_t>(row) * ldc + x;
@@ -173,6 +179,62 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
             if (c_row0 < M && x < N) tma_store_2d(tmap_c, staging + (c & 1) * kEpiBufBytes, x, c_row0);
             bulk_commit_group();  // an empty group keeps the per-buffer accounting uniform
         }
+    }
+}
+
+// ---------------------------------------------------------------- generic loads
+// For operands a tensor map cannot describe (a base that is not 16-byte
+// aligned, a row pitch that is not a multiple of 8 elements), the stages are
+// filled with plain loads by kLoaderThreads threads, in exactly the layout the
+// TMA unit would write: 16-byte chunks placed by the 128-byte swizzle (chunk
+// bits [4,7) of the shared-memory offset XOR bits [7,10)), zeros past M, N, K.
+// Each loader thread then makes its writes visible to the tensor cores
+// (fence.proxy.async) and arrives on the stage's full barrier.
+constexpr int kLoaderThreads = 128;
+
+__device__ __forceinline__ uint32_t swizzle128(uint32_t off) { return off ^ ((off >> 3) & 0x70u); }
+
+// Eight consecutive fp16 values from src (2-byte aligned); element e is read
+// only if e < avail (zero otherwise, and all zero when !row_ok).
+__device__ __forceinline__ uint4 load8_f16(const uint16_t* src, bool row_ok, int32_t avail)
+{
+    if (!row_ok || avail <= 0) return make_uint4(0u, 0u, 0u, 0u);
+    if (avail >= 8 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) return __ldg(reinterpret_cast<const uint4*>(src));
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = (2 * i < avail) ? __ldg(src + 2 * i) : 0u;
+        const uint32_t hi = (2 * i + 1 < avail) ? __ldg(src + 2 * i + 1) : 0u;
+        w[i] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One stage: A rows m0.. (TM x 64, K-major, rows of 128 B) and B rows k0..
+// (64 x TN, N-major, 64-column boxes of 64 rows x 128 B), as the TMA loads of
+// the same stage would leave them. lt = loader thread index.
+template <int TM, int TN>
+__device__ __forceinline__ void load_stage_generic(const GemmParams& p, uint32_t a_stage, uint32_t b_stage, int32_t m0,
+                                                   int32_t n0, int32_t k0, int lt)
+{
+    constexpr int TK = 64;
+    constexpr int A_ROW_CHUNKS = TK / 8;
+#pragma unroll 4
+    for (int q = lt; q < TM * A_ROW_CHUNKS; q += kLoaderThreads) {
+        const int r = q / A_ROW_CHUNKS, c = q % A_ROW_CHUNKS;
+        const int32_t gm = m0 + r, gk = k0 + 8 * c;
+        const uint4 v = load8_f16(p.A + static_cast<int64_t>(gm) * p.lda + gk, gm < p.M, p.K - gk);
+        st_shared_v4(a_stage + swizzle128(static_cast<uint32_t>(r * TK * 2 + c * 16)), v.x, v.y, v.z, v.w);
+    }
+    constexpr int B_ROW_CHUNKS = TN / 8;
+    constexpr uint32_t B_BOX = TK * 128;
+#pragma unroll 4
+    for (int q = lt; q < TK * B_ROW_CHUNKS; q += kLoaderThreads) {
+        const int k = q / B_ROW_CHUNKS, c = q % B_ROW_CHUNKS;
+        const int32_t gk = k0 + k, gn = n0 + 8 * c;
+        const uint4 v = load8_f16(p.B + static_cast<int64_t>(gk) * p.ldb + gn, gk < p.K, p.N - gn);
+        const uint32_t off = static_cast<uint32_t>(c >> 3) * B_BOX + static_cast<uint32_t>(k * 128 + (c & 7) * 16);
+        st_shared_v4(b_stage + swizzle128(off), v.x, v.y, v.z, v.w);
     }
 }
 

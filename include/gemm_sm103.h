@@ -54,10 +54,11 @@ extern "C" {
 typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = 1, /* negative extent, group_size_m <= 0, NULL with work to do, aliasing */
-    GEMM_ERR_UNSUPPORTED = 2, /* a TMA constraint: pointer not 16-byte aligned, a row pitch not a
-                                 multiple of 8 elements (for the contiguous entry points: N or
-                                 K not a multiple of 8), an extent above 2^30, an unknown tile
-                                 config */
+    GEMM_ERR_UNSUPPORTED = 2, /* a pointer that is not 2-byte aligned (not an fp16 address), an
+                                 extent or pitch above 2^30, an unknown tile config; for
+                                 gemm_f16_f32acc_noalloc also any operand a tensor map cannot
+                                 describe (a base not 16-byte aligned, N or K not a multiple
+                                 of 8) */
     GEMM_ERR_CUDA = 3,        /* a CUDA runtime call failed (see gemm_last_cuda_error) */
     GEMM_ERR_TIMEOUT = 4      /* a kernel's bounded wait expired (reported by gemm_query_status) */
 } gemm_status_t;
@@ -76,12 +77,16 @@ typedef enum {
 /*
  * C = A * B, fp16 in, fp32 accumulate, fp16 out (see the header comment).
  *
- *   A            device, fp16 [M,K] row-major; 16-byte aligned
- *   B            device, fp16 [K,N] row-major; 16-byte aligned
- *   C            device, fp16 [M,N] row-major; 16-byte aligned; must not
+ *   A            device, fp16 [M,K] row-major; 2-byte aligned
+ *   B            device, fp16 [K,N] row-major; 2-byte aligned
+ *   C            device, fp16 [M,N] row-major; 2-byte aligned; must not
  *                overlap A or B. Fully overwritten.
- *   M, N, K      extents, 0 <= M, N, K <= 2^30; N % 8 == 0 and K % 8 == 0
- *                (row pitches must be multiples of 16 bytes for TMA)
+ *   M, N, K      extents, 0 <= M, N, K <= 2^30
+ *   Operands whose bases are 16-byte aligned and whose row pitches (here K
+ *   for A, N for B and C) are multiples of 8 elements run the TMA kernels;
+ *   any other operands run a generic kernel that fills the same shared-memory
+ *   stages with plain loads and writes C with direct stores (the same tensor
+ *   core path and result; 128x256x64 tiles, whatever tile_cfg asks for).
  *   group_size_m GROUP_SIZE_M of the grouped tile order, >= 1. Values above
  *                num_pid_m give the same order as num_pid_m.
  *   stream       cudaStream_t
@@ -119,12 +124,13 @@ int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int6
  *   element (i,k) of A at A + i*lda + k,  (k,j) of B at B + k*ldb + j,
  *   element (i,j) of C at C + i*ldc + j.
  *
- *   lda >= K, ldb >= N, ldc >= N, each a multiple of 8 elements (16 bytes) and
- *   at most 2^30; A, B, C 16-byte aligned. M, N, K need no alignment: loads
- *   past the extents read zeros and stores stop at column N, so the padding
- *   columns [N, ldc) of C are never written. Errors as for gemm_f16_f32acc
- *   (a pitch below its row length is GEMM_ERR_INVALID_ARG, a misaligned pitch
- *   GEMM_ERR_UNSUPPORTED). Column strides other than 1 are not supported.
+ *   lda >= K, ldb >= N, ldc >= N, each at most 2^30; A, B, C 2-byte aligned.
+ *   Pitches that are multiples of 8 elements with 16-byte aligned bases take
+ *   the TMA kernels, any others the generic-load kernel (gemm_f16_f32acc).
+ *   M, N, K need no alignment: loads past the extents read zeros and stores
+ *   stop at column N, so the padding columns [N, ldc) of C are never written.
+ *   Errors as for gemm_f16_f32acc (a pitch below its row length is
+ *   GEMM_ERR_INVALID_ARG). Column strides other than 1 are not supported.
  */
 int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t M,
                             int64_t N, int64_t K, int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace,
@@ -217,7 +223,10 @@ uint64_t gemm_launch_count(void);
  * present on every GPU that loads the library until the process exits.
  *
  *   A, B, C, M, N, K, group_size_m, stream
- *              as for gemm_f16_f32acc, with the same validation and errors
+ *              as for gemm_f16_f32acc, with the same validation and errors,
+ *              except that operands a tensor map cannot describe (bases not
+ *              16-byte aligned, N or K not a multiple of 8) give
+ *              GEMM_ERR_UNSUPPORTED: this entry point has no generic kernel
  *   d_status   NULL, or a device uint32_t that receives, in stream order after
  *              the kernel, this call's status word: 0 = complete, bit 0 set =
  *              a bounded wait expired (the output is then incomplete)

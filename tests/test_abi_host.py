@@ -64,11 +64,9 @@ def test_validation_without_gpu(lib):
     assert _call(lib, G=-3) == inv
     assert _call(lib, C=0) == inv                       # NULL C with work to do
     assert _call(lib, A=0) == inv                       # NULL A with K > 0
-    assert _call(lib, A=24) == uns                      # 8-byte aligned only
-    assert _call(lib, B=big + 2) == uns
-    assert _call(lib, C=big + 8) == uns
-    assert _call(lib, N=60) == uns                      # row pitch not a multiple of 16 B
-    assert _call(lib, K=100) == uns
+    assert _call(lib, A=25) == uns                      # fp16 needs 2-byte aligned bases
+    assert _call(lib, B=big + 1) == uns
+    assert _call(lib, C=big + 3) == uns
     assert _call(lib, M=(1 << 30) + 1) == uns
     assert _call(lib, cfg=99) == uns
     # C overlapping A or B
@@ -112,13 +110,13 @@ def test_strided_validation_without_gpu(lib):
     assert _strided(lib, lda=56) == inv            # pitch shorter than the row
     assert _strided(lib, ldb=63) == inv
     assert _strided(lib, ldc=8) == inv
-    assert _strided(lib, lda=68) == uns            # pitch not a multiple of 8 elements
-    assert _strided(lib, ldc=100) == uns
     assert _strided(lib, ldb=(1 << 30) + 8) == uns
     assert _strided(lib, A=big, lda=1024, B=2 * big, C=big + 1024 * 2 * 63, ldc=1024) == inv  # C inside A's rows
     assert _strided(lib, M=0, A=0, B=0, C=0) == g.GEMM_OK
-    # the contiguous entry point keeps its N % 8, K % 8 rule through the pitch rule
-    assert lib.gemm_f16_f32acc(16, 16, 16, 64, 60, 64, 8, None) == uns
+    assert _strided(lib, A=big + 1, lda=67) == uns     # odd base: not an fp16 address
+    # the no-alloc entry point keeps the tensor-map rules (16-byte bases, pitches of 8 elements)
+    assert lib.gemm_f16_f32acc_noalloc(16, big, 2 * big, 64, 60, 64, 8, None, None) == uns
+    assert lib.gemm_f16_f32acc_noalloc(18, big, 2 * big, 64, 64, 64, 8, None, None) == uns
 
 
 def test_python_binding_accepts_padded_rows_only(lib):

@@ -182,3 +182,71 @@ def test_strided_k_zero_stops_at_n(gemm_lib):
     g.gemm(a, b, out=c_buf.view(torch.float16)[:, :N])
     assert g.query_status() == g.GEMM_OK
     assert torch.all(c_buf[:, :N] == 0) and torch.all(c_buf[:, N:] == 0x7E01)
+
+
+# ---- operands a tensor map cannot describe: the generic-load kernel
+# (bases 2-byte aligned only, row pitches that are not multiples of 8)
+GENERIC = [
+    # M, N, K, lda, ldb, ldc, element offsets of the A, B, C bases
+    (300, 999, 1001, 1001, 999, 999, 0, 0, 0),     # contiguous, odd N and K
+    (129, 264, 72, 75, 270, 267, 0, 0, 0),        # odd pitches, aligned extents
+    (300, 520, 264, 264, 520, 520, 1, 3, 5),      # TMA-shaped pitches, bases off by 2/6/10 bytes
+    (257, 300, 77, 79, 301, 303, 7, 1, 1),        # everything odd
+    (1, 8, 8, 8, 8, 8, 1, 1, 1),
+    (1000, 37, 1000, 1003, 37, 41, 0, 0, 0),      # narrow N
+    (2048, 2048, 2000, 2001, 2049, 2051, 1, 1, 1),  # several tiles per CTA, K > 512
+]
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,oa,ob,oc", GENERIC)
+def test_generic_load_path(gemm_lib, M, N, K, lda, ldb, ldc, oa, ob, oc):
+    A, B = inputs.gemm_inputs(M, N, K, seed=M + 5 * N + 11 * K)
+    nan = float("nan")
+    a_buf = torch.full((oa + M * lda,), nan, dtype=torch.float16)
+    b_buf = torch.full((ob + K * ldb,), nan, dtype=torch.float16)
+    a_buf[oa:].view(M, lda)[:, :K] = A
+    b_buf[ob:].view(K, ldb)[:, :N] = B
+    canary = 0x7E01
+    pad = 64
+    c_buf = torch.full((pad + oc + M * ldc + pad,), canary, dtype=torch.int16, device="cuda")
+    a_view = a_buf.cuda()[oa:].view(M, lda)[:, :K]
+    b_view = b_buf.cuda()[ob:].view(K, ldb)[:, :N]
+    c_view = c_buf[pad + oc:pad + oc + M * ldc].view(torch.float16).view(M, ldc)[:, :N]
+    n0 = g.launch_count()
+    g.gemm(a_view, b_view, out=c_view)       # the NaN padding of A and B is never read
+    assert g.query_status() == g.GEMM_OK
+    assert g.launch_count() - n0 == 1
+    check_against_oracle(A, B, c_view.contiguous())
+    assert torch.all(c_buf[:pad + oc] == canary) and torch.all(c_buf[pad + oc + M * ldc:] == canary)
+    if ldc > N:
+        assert torch.all(c_buf[pad + oc:pad + oc + M * ldc].view(M, ldc)[:, N:] == canary)
+
+
+def test_generic_path_small_integers_exact(gemm_lib):
+    M, N, K = 200, 301, 517
+    gen = torch.Generator().manual_seed(9)
+    A = torch.randint(-4, 5, (M, K), generator=gen).half()
+    B = torch.randint(-4, 5, (K, N), generator=gen).half()
+    C = g.gemm(A.cuda(), B.cuda())         # K and N odd: contiguous pitches are not multiples of 8
+    want = (A.double() @ B.double())
+    assert torch.all(want.abs() <= 2048)
+    assert torch.equal(C.cpu().double(), want)
+
+
+def test_generic_path_k_zero_and_matches_tma_path(gemm_lib):
+    # K == 0 through the generic kernel (odd ldc)
+    M, N, ldc = 130, 99, 101
+    c_buf = torch.full((M, ldc), 0x7E01, dtype=torch.int16, device="cuda")
+    g.gemm(torch.empty((M, 0), dtype=torch.float16, device="cuda"),
+           torch.empty((0, N), dtype=torch.float16, device="cuda"), out=c_buf.view(torch.float16)[:, :N])
+    assert g.query_status() == g.GEMM_OK
+    assert torch.all(c_buf[:, :N] == 0) and torch.all(c_buf[:, N:] == 0x7E01)
+    # the same problem through both kernels: identical bits (same MMA order per 64-deep k step)
+    M, N, K = 384, 512, 640
+    A, B = inputs.gemm_inputs(M, N, K, seed=77)
+    a, b = A.cuda(), B.cuda()
+    c_tma = g.gemm(a, b, tile_cfg=g.TILE_128x256x64)
+    a_off = torch.empty(M * K + 1, dtype=torch.float16, device="cuda")
+    a_off[1:] = a.reshape(-1)
+    c_gen = g.gemm(a_off[1:].view(M, K), b)          # A 2 bytes off a 16-byte boundary
+    assert torch.equal(c_tma, c_gen)

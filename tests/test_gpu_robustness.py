@@ -21,10 +21,15 @@ pytestmark = pytest.mark.gpu
 CANARY = 0x7E01  # a quiet-NaN fp16 bit pattern the kernel never produces from finite inputs
 
 
-@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR])
+@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR,
+                                 "generic"])
 def test_watchdog_timeout_reports_and_recovers(gemm_lib, cfg):
     A, B = inputs.gemm_inputs(256, 512, 128, seed=41)
     a, b = A.cuda(), B.cuda()
+    if cfg == "generic":  # A one element off a 16-byte boundary: the generic-load kernel
+        buf = torch.empty(A.numel() + 1, dtype=torch.float16, device="cuda")
+        buf[1:] = a.reshape(-1)
+        a, cfg = buf[1:].view(A.shape), g.TILE_AUTO
     assert g.query_status() == g.GEMM_OK
     try:
         g.set_watchdog_ns(50_000_000)  # 50 ms
@@ -41,7 +46,7 @@ def test_watchdog_timeout_reports_and_recovers(gemm_lib, cfg):
 
 
 @pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR])
-@pytest.mark.parametrize("M,N,K", [(129, 264, 72), (4095, 3000, 1000), (1, 8, 8), (300, 8, 1000)])
+@pytest.mark.parametrize("M,N,K", [(129, 264, 72), (4095, 3000, 1000), (1, 8, 8), (300, 8, 1000), (300, 999, 1001)])
 def test_no_store_outside_c(gemm_lib, M, N, K, cfg):
     A, B = inputs.gemm_inputs(M, N, K, seed=M + N + K)
     pad = 4096  # elements before and after C (multiple of 8: C stays 16-byte aligned)
@@ -59,14 +64,16 @@ def test_device_pointer_errors(gemm_lib):
     b = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
     c = torch.zeros((64 * 64 + 8,), dtype=torch.float16, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
-    # C at a 2-byte offset: not 16-byte aligned
-    rc = lib.gemm_f16_f32acc(a.data_ptr(), b.data_ptr(), c.data_ptr() + 2, 64, 64, 64, 8, s)
+    # C at a 1-byte offset: not an fp16 address
+    rc = lib.gemm_f16_f32acc(a.data_ptr(), b.data_ptr(), c.data_ptr() + 1, 64, 64, 64, 8, s)
     assert rc == g.GEMM_ERR_UNSUPPORTED
     # C aliasing A
     rc = lib.gemm_f16_f32acc(a.data_ptr(), b.data_ptr(), a.data_ptr(), 64, 64, 64, 8, s)
     assert rc == g.GEMM_ERR_INVALID_ARG
-    with pytest.raises(g.GemmError):
-        g.gemm(a[:, :60].contiguous(), b[:60].contiguous())  # K = 60: not a multiple of 8
+    # C at a 2-byte offset, K = 60: the generic-load kernel runs them
+    rc = lib.gemm_f16_f32acc(a.data_ptr(), b.data_ptr(), c.data_ptr() + 2, 64, 64, 64, 8, s)
+    assert rc == g.GEMM_OK
+    g.gemm(a[:, :60].contiguous(), b[:60].contiguous())
     assert g.query_status() == g.GEMM_OK
 
 
