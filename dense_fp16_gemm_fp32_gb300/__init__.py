@@ -38,5 +38,6 @@ from ._binding import (  # noqa: F401
     status_string,
     tile_schedule,
     tile_shape,
+    workspace_bytes,
 )
 from ._build import build  # noqa: F401

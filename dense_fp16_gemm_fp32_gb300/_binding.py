@@ -65,6 +65,13 @@ _SIGNATURES = {
     "gemm_launch_count": (ctypes.c_uint64, []),
     "gemm_f16_f32acc_noalloc": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, ctypes.c_int64, ctypes.c_int64,
                                                ctypes.c_int64, ctypes.c_int32, _c_void_p, _c_void_p]),
+    "gemm_workspace_bytes": (ctypes.c_int, [_c_void_p, ctypes.c_int64, _c_void_p, ctypes.c_int64, _c_void_p,
+                                            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                            _c_void_p]),
+    "gemm_f16_f32acc_strided_ws": (ctypes.c_int, [_c_void_p, ctypes.c_int64, _c_void_p, ctypes.c_int64, _c_void_p,
+                                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                  ctypes.c_int32, ctypes.c_int32, _c_void_p, _c_void_p,
+                                                  ctypes.c_uint64, _c_void_p]),
     "softmax_rows_f32": (ctypes.c_int, [_c_void_p, ctypes.c_int64, _c_void_p, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.c_int64, _c_void_p]),
     "softmax_rows_plan": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, _c_void_p, _c_void_p, _c_void_p]),
@@ -154,13 +161,16 @@ def _ld(t: torch.Tensor) -> int:
 
 def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZE_M,
          out: torch.Tensor | None = None, tile_cfg: int = TILE_AUTO,
-         trace: torch.Tensor | None = None) -> torch.Tensor:
+         trace: torch.Tensor | None = None, repack: bool = True) -> torch.Tensor:
     """C = a @ b with fp16 operands, fp32 accumulation and one fp16 rounding.
 
     a: [M,K] fp16 CUDA row-major; b: [K,N] fp16 CUDA row-major, same device.
     Row-major views with padded rows (stride (ld, 1), ld >= columns) are
     accepted with any pitch: pitches that are multiples of 8 elements with
-    16-byte aligned data run the TMA kernels, others a plain-load kernel.
+    16-byte aligned data run the TMA kernels in place. Other operands are
+    copied into a workspace allocated here (repack=True, the default) and
+    the TMA kernels run on the copies; with repack=False they run through
+    the library's plain-load kernel instead.
     out: optional [M,N] fp16 CUDA row-major tensor (or padded view) to write;
     its padding columns are not touched.
     trace: optional int32 CUDA tensor of 3 * num_tiles entries that receives
@@ -187,11 +197,20 @@ def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZ
             raise ValueError("trace must be a contiguous int32 tensor on a's device")
         trace_ptr = trace.data_ptr()
     lib = load()
+    args = (a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(), _ld(out), M, N, K)
     with torch.cuda.device(a.device):
-        rc = lib.gemm_f16_f32acc_strided(a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(), _ld(out),
-                                         M, N, K, int(group_size_m), int(tile_cfg), trace_ptr,
-                                         _stream_ptr(a.device))
-    _check(rc, "gemm_f16_f32acc_strided")
+        need = ctypes.c_uint64(0)
+        if repack:
+            _check(lib.gemm_workspace_bytes(*args, ctypes.byref(need)), "gemm_workspace_bytes")
+        if need.value:
+            ws = torch.empty(need.value, dtype=torch.uint8, device=a.device)  # caching allocator: stream-ordered reuse
+            rc = lib.gemm_f16_f32acc_strided_ws(*args, int(group_size_m), int(tile_cfg), trace_ptr, ws.data_ptr(),
+                                                need.value, _stream_ptr(a.device))
+            _check(rc, "gemm_f16_f32acc_strided_ws")
+        else:
+            rc = lib.gemm_f16_f32acc_strided(*args, int(group_size_m), int(tile_cfg), trace_ptr,
+                                             _stream_ptr(a.device))
+            _check(rc, "gemm_f16_f32acc_strided")
     return out
 
 
@@ -310,3 +329,13 @@ def softmax_plan(M: int, n: int, device=None) -> dict:
 
 def softmax_launch_count() -> int:
     return int(load().softmax_launch_count())
+
+
+def workspace_bytes(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor) -> int:
+    """Workspace gemm() allocates for these operands (0 when all suit the TMA kernels)."""
+    need = ctypes.c_uint64(0)
+    M, K = a.shape
+    N = b.shape[1]
+    _check(load().gemm_workspace_bytes(a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(), _ld(out), M, N, K,
+                                       ctypes.byref(need)), "gemm_workspace_bytes")
+    return int(need.value)

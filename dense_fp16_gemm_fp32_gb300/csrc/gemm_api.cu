@@ -448,9 +448,127 @@ int noalloc_setup(NoAllocDeviceState** out)
     return GEMM_OK;
 }
 
+// ---------------------------------------------------------------- workspace repacking
+// Operands that fail the tensor-map rules can be copied into a caller's
+// workspace with 16-byte aligned rows and pitches of a multiple of 8 elements;
+// the TMA kernels then run on the copies, and a C copy is written back.
+constexpr uint64_t kWsAlign = 256;
+
+int64_t round_up8(int64_t x) { return (x + 7) / 8 * 8; }
+uint64_t round_up_ws(uint64_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+bool operand_tma_ok(const void* ptr, int64_t ld) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0 && (ld & 7) == 0; }
+
+struct WsLayout {
+    bool rep_a, rep_b, rep_c;
+    uint64_t off_a, off_b, off_c, bytes;
+};
+
+WsLayout ws_layout(const Problem& pr)
+{
+    WsLayout w{};
+    w.rep_a = pr.K > 0 && !operand_tma_ok(pr.A, pr.lda);
+    w.rep_b = pr.K > 0 && !operand_tma_ok(pr.B, pr.ldb);
+    w.rep_c = !operand_tma_ok(pr.C, pr.ldc);
+    uint64_t off = 0;
+    if (w.rep_a) w.off_a = off, off = round_up_ws(off + static_cast<uint64_t>(pr.M) * round_up8(pr.K) * 2);
+    if (w.rep_b) w.off_b = off, off = round_up_ws(off + static_cast<uint64_t>(pr.K) * round_up8(pr.N) * 2);
+    if (w.rep_c) w.off_c = off, off = round_up_ws(off + static_cast<uint64_t>(pr.M) * round_up8(pr.N) * 2);
+    w.bytes = off;
+    return w;
+}
+
+int launch_copy(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows, int64_t cols, cudaStream_t s)
+{
+    DeviceState* d = nullptr;
+    const int rc = device_state(&d);
+    if (rc != GEMM_OK) return rc;
+    const int64_t want = static_cast<int64_t>(d->sm_count) * 8;
+    const unsigned grid = static_cast<unsigned>(rows < want ? rows : want);
+    copy_rows_f16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(src), lds, static_cast<uint16_t*>(dst),
+                                                ldd, static_cast<int32_t>(rows), static_cast<int32_t>(cols));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
+// The TMA kernels for a validated problem whose operands suit them.
+int dispatch_tma(const Problem& pr, int cfg, int32_t* trace, cudaStream_t s)
+{
+    switch (cfg) {
+        case GEMM_TILE_128x64x32:
+            return launch<Cfg128x64>(pr, cfg, trace, s);
+        case GEMM_TILE_256x256x64_PAIR:
+            return launch_pair<CfgPair256>(pr, cfg, trace, s);
+        case GEMM_TILE_256x256x128_PAIR:
+            return launch_pair<CfgPair256Deep>(pr, cfg, trace, s);
+        default:
+            return launch<Cfg128x256>(pr, cfg, trace, s);
+    }
+}
+
 }  // namespace
 
 extern "C" {
+
+int gemm_workspace_bytes(const void* A, int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc,
+                         int64_t M, int64_t N, int64_t K, uint64_t* bytes)
+{
+    if (bytes == nullptr) return GEMM_ERR_INVALID_ARG;
+    *bytes = 0;
+    const Problem pr{A, B, const_cast<void*>(C), M, N, K, 1, lda, ldb, ldc};
+    const int rc = validate(pr);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    *bytes = ws_layout(pr).bytes;
+    return GEMM_OK;
+}
+
+int gemm_f16_f32acc_strided_ws(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                               int64_t M, int64_t N, int64_t K, int32_t group_size_m, int32_t tile_cfg,
+                               int32_t* tile_trace, void* workspace, uint64_t workspace_bytes, void* stream)
+{
+    const Problem pr{A, B, C, M, N, K, group_size_m, lda, ldb, ldc};
+    int32_t tm, tn, tk;
+    const int cfg = resolve_cfg(tile_cfg, M, &tm, &tn, &tk);
+    if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
+    int rc = validate(pr);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (tma_ok(pr)) return dispatch_tma(pr, cfg, tile_trace, s);
+    const WsLayout w = ws_layout(pr);
+    const uintptr_t ws = reinterpret_cast<uintptr_t>(workspace);
+    if (workspace == nullptr || workspace_bytes < w.bytes || (ws & (kWsAlign - 1)) != 0)
+        return launch<CfgGeneric>(pr, kGenericCfgId, tile_trace, s);
+    // the workspace must not overlap an operand
+    using u128 = unsigned __int128;
+    const u128 ws_end = static_cast<u128>(ws) + w.bytes;
+    auto overlaps = [&](const void* p, int64_t rows, int64_t ld, int64_t cols) {
+        const uintptr_t b = reinterpret_cast<uintptr_t>(p);
+        const u128 e = static_cast<u128>(b) + (static_cast<u128>(rows - 1) * ld + cols) * 2;
+        return ws < e && b < ws_end;
+    };
+    if (overlaps(C, M, ldc, N) || (K > 0 && (overlaps(A, M, lda, K) || overlaps(B, K, ldb, N))))
+        return GEMM_ERR_INVALID_ARG;
+
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    Problem q = pr;
+    if (w.rep_a) {
+        q.A = base + w.off_a, q.lda = round_up8(K);
+        rc = launch_copy(A, lda, base + w.off_a, q.lda, M, K, s);
+        if (rc != GEMM_OK) return rc;
+    }
+    if (w.rep_b) {
+        q.B = base + w.off_b, q.ldb = round_up8(N);
+        rc = launch_copy(B, ldb, base + w.off_b, q.ldb, K, N, s);
+        if (rc != GEMM_OK) return rc;
+    }
+    if (w.rep_c) q.C = base + w.off_c, q.ldc = round_up8(N);
+    rc = dispatch_tma(q, cfg, tile_trace, s);
+    if (rc != GEMM_OK) return rc;
+    if (w.rep_c) return launch_copy(q.C, q.ldc, C, ldc, M, N, s);
+    return GEMM_OK;
+}
 
 int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t M,
                             int64_t N, int64_t K, int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace,
@@ -464,16 +582,7 @@ int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t l
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!tma_ok(pr)) return launch<CfgGeneric>(pr, kGenericCfgId, tile_trace, s);
-    switch (cfg) {
-        case GEMM_TILE_128x64x32:
-            return launch<Cfg128x64>(pr, cfg, tile_trace, s);
-        case GEMM_TILE_256x256x64_PAIR:
-            return launch_pair<CfgPair256>(pr, cfg, tile_trace, s);
-        case GEMM_TILE_256x256x128_PAIR:
-            return launch_pair<CfgPair256Deep>(pr, cfg, tile_trace, s);
-        default:
-            return launch<Cfg128x256>(pr, cfg, tile_trace, s);
-    }
+    return dispatch_tma(pr, cfg, tile_trace, s);
 }
 
 int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,

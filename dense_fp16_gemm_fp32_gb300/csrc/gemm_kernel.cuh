@@ -11,7 +11,7 @@
 // (tile_map.cuh).
 //
 // GB300 mapping (one CTA of 192 threads per SM, persistent over tiles; the
-// generic-load form adds loader warps 6..8, see TileCfg):
+// generic-load form adds loader warps 6..12, see TileCfg):
 //   warp 0           TMA producer (lane 0 issues): per k step, one A box (TILE_K x TILE_M,
 //                    K contiguous) and TILE_N/64 B boxes (64 x TILE_K, N
 //                    contiguous) into an S-stage shared-memory ring, tracked by
@@ -47,8 +47,8 @@
 namespace gemm103 {
 
 // kGeneric: the stages are filled by plain loads (load_stage_generic) from
-// warps 0, 6, 7 and 8 instead of TMA, and C is written with direct stores,
-// for operands whose base or row pitch a tensor map cannot describe.
+// warps 0 and 6..12 instead of TMA, and C is written with direct stores, for
+// operands whose base or row pitch a tensor map cannot describe.
 template <int TM_, int TN_, int TK_, int STAGES_, bool kGeneric_ = false>
 struct TileCfg {
     static constexpr int TM = TM_, TN = TN_, TK = TK_, STAGES = STAGES_;
@@ -58,7 +58,7 @@ struct TileCfg {
     static_assert(TK == 64 || TK == 32, "A rows of 128 B (128B swizzle) or 64 B (64B swizzle)");
     static_assert(!kGeneric || TK == 64, "generic loads write the 128-byte swizzle");
 
-    static constexpr int NUM_THREADS = kGeneric ? 192 + 96 : 192;
+    static constexpr int NUM_THREADS = kGeneric ? 192 + kLoaderThreads - 32 : 192;
     static constexpr int FULL_ARRIVALS = kGeneric ? kLoaderThreads : 1;
     static constexpr int EPI_THREADS = 128;
 
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
     if (Cfg::kGeneric && (warp == 0 || warp >= 6)) {
         // ------------------------------------------------------------ generic loaders
-        // Four warps fill each stage with plain loads; every thread arrives on
+        // Eight warps fill each stage with plain loads; every thread arrives on
         // the stage's full barrier after its writes (kLoaderThreads arrivals).
         const int lt = (warp == 0 ? 0 : warp - 5) * 32 + lane;
         if (p.num_k_tiles > 0 && p.fault_mode != 1) {
@@ -307,6 +307,44 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+// Eight consecutive fp16 values to dst (2-byte aligned); element e is
+// written only if e < avail. The widest stores dst's alignment allows.
+__device__ __forceinline__ void store8_f16(uint16_t* dst, uint4 v, int32_t avail)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+    if (avail >= 8 && (a & 15u) == 0) {
+        *reinterpret_cast<uint4*>(dst) = v;
+        return;
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (avail >= 8 && (a & 3u) == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) reinterpret_cast<uint32_t*>(dst)[i] = w[i];
+        return;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        if (e < avail) dst[e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+}
+
+// Row-by-row copy of an fp16 matrix between two row pitches (either side may
+// be any 2-byte aligned address and pitch): dst[r*ldd + c] = src[r*lds + c]
+// for r < rows, c < cols. Used to repack operands a tensor map cannot describe
+// into a caller-provided workspace, and to copy C back out of it. HBM-bound:
+// each thread moves runs of 8 elements with the widest loads and stores the
+// two sides' alignment allows; CTAs take rows in a grid stride.
+__global__ void __launch_bounds__(256) copy_rows_f16_kernel(const uint16_t* __restrict__ src, int64_t lds,
+                                                            uint16_t* __restrict__ dst, int64_t ldd, int32_t rows,
+                                                            int32_t cols)
+{
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const uint16_t* s = src + r * lds;
+        uint16_t* d = dst + r * ldd;
+        for (int32_t c = 8 * static_cast<int32_t>(threadIdx.x); c < cols; c += 8 * static_cast<int32_t>(blockDim.x))
+            store8_f16(d + c, load8_f16(s + c, true, cols - c), cols - c);
     }
 }
 

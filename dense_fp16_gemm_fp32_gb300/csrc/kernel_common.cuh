@@ -188,9 +188,11 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
 // filled with plain loads by kLoaderThreads threads, in exactly the layout the
 // TMA unit would write: 16-byte chunks placed by the 128-byte swizzle (chunk
 // bits [4,7) of the shared-memory offset XOR bits [7,10)), zeros past M, N, K.
-// Each loader thread then makes its writes visible to the tensor cores
-// (fence.proxy.async) and arrives on the stage's full barrier.
-constexpr int kLoaderThreads = 128;
+// Each loader thread issues all of its loads of a stage before its first
+// shared-memory store (one memory round trip per stage), then makes its
+// writes visible to the tensor cores (fence.proxy.async) and arrives on the
+// stage's full barrier.
+constexpr int kLoaderThreads = 256;
 
 __device__ __forceinline__ uint32_t swizzle128(uint32_t off) { return off ^ ((off >> 3) & 0x70u); }
 
@@ -199,13 +201,19 @@ __device__ __forceinline__ uint32_t swizzle128(uint32_t off) { return off ^ ((of
 __device__ __forceinline__ uint4 load8_f16(const uint16_t* src, bool row_ok, int32_t avail)
 {
     if (!row_ok || avail <= 0) return make_uint4(0u, 0u, 0u, 0u);
-    if (avail >= 8 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) return __ldg(reinterpret_cast<const uint4*>(src));
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+    if (avail >= 8 && (a & 15u) == 0) return __ldg(reinterpret_cast<const uint4*>(src));
     uint32_t w[4];
+    if (avail >= 8 && (a & 3u) == 0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = (2 * i < avail) ? __ldg(src + 2 * i) : 0u;
-        const uint32_t hi = (2 * i + 1 < avail) ? __ldg(src + 2 * i + 1) : 0u;
-        w[i] = lo | (hi << 16);
+        for (int i = 0; i < 4; ++i) w[i] = __ldg(reinterpret_cast<const uint32_t*>(src) + i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = (2 * i < avail) ? __ldg(src + 2 * i) : 0u;
+            const uint32_t hi = (2 * i + 1 < avail) ? __ldg(src + 2 * i + 1) : 0u;
+            w[i] = lo | (hi << 16);
+        }
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -219,22 +227,40 @@ __device__ __forceinline__ void load_stage_generic(const GemmParams& p, uint32_t
 {
     constexpr int TK = 64;
     constexpr int A_ROW_CHUNKS = TK / 8;
-#pragma unroll 4
-    for (int q = lt; q < TM * A_ROW_CHUNKS; q += kLoaderThreads) {
+    constexpr int B_ROW_CHUNKS = TN / 8;
+    constexpr int A_PER = TM * A_ROW_CHUNKS / kLoaderThreads;
+    constexpr int B_PER = TK * B_ROW_CHUNKS / kLoaderThreads;
+    static_assert(A_PER * kLoaderThreads == TM * A_ROW_CHUNKS && B_PER * kLoaderThreads == TK * B_ROW_CHUNKS,
+                  "whole chunks per loader thread");
+    constexpr uint32_t B_BOX = TK * 128;
+    uint4 va[A_PER], vb[B_PER];
+#pragma unroll
+    for (int i = 0; i < A_PER; ++i) {
+        const int q = lt + kLoaderThreads * i;
         const int r = q / A_ROW_CHUNKS, c = q % A_ROW_CHUNKS;
         const int32_t gm = m0 + r, gk = k0 + 8 * c;
-        const uint4 v = load8_f16(p.A + static_cast<int64_t>(gm) * p.lda + gk, gm < p.M, p.K - gk);
-        st_shared_v4(a_stage + swizzle128(static_cast<uint32_t>(r * TK * 2 + c * 16)), v.x, v.y, v.z, v.w);
+        va[i] = load8_f16(p.A + static_cast<int64_t>(gm) * p.lda + gk, gm < p.M, p.K - gk);
     }
-    constexpr int B_ROW_CHUNKS = TN / 8;
-    constexpr uint32_t B_BOX = TK * 128;
-#pragma unroll 4
-    for (int q = lt; q < TK * B_ROW_CHUNKS; q += kLoaderThreads) {
+#pragma unroll
+    for (int i = 0; i < B_PER; ++i) {
+        const int q = lt + kLoaderThreads * i;
         const int k = q / B_ROW_CHUNKS, c = q % B_ROW_CHUNKS;
         const int32_t gk = k0 + k, gn = n0 + 8 * c;
-        const uint4 v = load8_f16(p.B + static_cast<int64_t>(gk) * p.ldb + gn, gk < p.K, p.N - gn);
+        vb[i] = load8_f16(p.B + static_cast<int64_t>(gk) * p.ldb + gn, gk < p.K, p.N - gn);
+    }
+#pragma unroll
+    for (int i = 0; i < A_PER; ++i) {
+        const int q = lt + kLoaderThreads * i;
+        const int r = q / A_ROW_CHUNKS, c = q % A_ROW_CHUNKS;
+        st_shared_v4(a_stage + swizzle128(static_cast<uint32_t>(r * TK * 2 + c * 16)), va[i].x, va[i].y, va[i].z,
+                     va[i].w);
+    }
+#pragma unroll
+    for (int i = 0; i < B_PER; ++i) {
+        const int q = lt + kLoaderThreads * i;
+        const int k = q / B_ROW_CHUNKS, c = q % B_ROW_CHUNKS;
         const uint32_t off = static_cast<uint32_t>(c >> 3) * B_BOX + static_cast<uint32_t>(k * 128 + (c & 7) * 16);
-        st_shared_v4(b_stage + swizzle128(off), v.x, v.y, v.z, v.w);
+        st_shared_v4(b_stage + swizzle128(off), vb[i].x, vb[i].y, vb[i].z, vb[i].w);
     }
 }
 

@@ -137,6 +137,40 @@ int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t l
                             void* stream);
 
 /*
+ * Bytes of workspace gemm_f16_f32acc_strided_ws needs to run these operands
+ * through the TMA kernels (host-only, no device work): 0 when every operand
+ * already suits them; otherwise room for a copy, with 16-byte aligned rows
+ * and a pitch rounded up to 8 elements, of each operand that does not (A:
+ * M x K, B: K x N, C: M x N), each copy 256-byte aligned. The pointers and
+ * pitches are only inspected, never dereferenced. Arguments are validated
+ * as for gemm_f16_f32acc_strided (same errors); bytes is a host pointer
+ * (NULL -> GEMM_ERR_INVALID_ARG).
+ */
+int gemm_workspace_bytes(const void* A, int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc,
+                         int64_t M, int64_t N, int64_t K, uint64_t* bytes);
+
+/*
+ * As gemm_f16_f32acc_strided, with a caller-owned device workspace for
+ * operands a tensor map cannot describe. When workspace is 256-byte aligned
+ * and holds at least gemm_workspace_bytes(...) bytes, each such operand is
+ * first copied into it (A and B; an HBM-bound row copy kernel), the TMA
+ * kernels run on the copies with tile_cfg, and a C copy is then written back
+ * to C (stream-ordered, all on `stream`). Otherwise (workspace NULL, too
+ * small or misaligned) the call runs the generic-load kernel exactly as
+ * gemm_f16_f32acc_strided does. Operands that already suit the TMA kernels
+ * are used in place and need no workspace.
+ *
+ *   workspace        device pointer or NULL; owned by the caller, must not
+ *                    overlap A, B or C (GEMM_ERR_INVALID_ARG), and must not
+ *                    be used by anything else until the call's work on
+ *                    `stream` has finished
+ *   workspace_bytes  its size in bytes
+ */
+int gemm_f16_f32acc_strided_ws(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                               int64_t M, int64_t N, int64_t K, int32_t group_size_m, int32_t tile_cfg,
+                               int32_t* tile_trace, void* workspace, uint64_t workspace_bytes, void* stream);
+
+/*
  * Tile shape a configuration uses for a problem (GEMM_TILE_AUTO depends on M): writes TILE_M, TILE_N,
  * TILE_K (host pointers, each may be NULL) and returns GEMM_OK, or
  * GEMM_ERR_UNSUPPORTED for an unknown tile_cfg. No device work.
@@ -206,7 +240,9 @@ int gemm_set_watchdog_ns(uint64_t ns);
  */
 int gemm_set_fault_injection(int32_t mode);
 
-/* Number of kernels this library has launched in this process (all devices). */
+/* Number of kernels the GEMM entry points (the workspace copies included) and
+ * gemm_tile_schedule have launched in this process, all devices. The row
+ * softmax keeps its own count (softmax_launch_count). */
 uint64_t gemm_launch_count(void);
 
 /*

@@ -172,3 +172,26 @@ def test_python_softmax_rejects_bad_tensors(lib):
         g.softmax(torch.zeros((4, 8), dtype=torch.float16))
     assert g._binding._row_pitch(torch.zeros((1, 5))) == 8
     assert g._binding._row_pitch(torch.zeros((3, 16))[:, :5]) == 16
+
+
+def test_workspace_bytes_without_gpu(lib):
+    big = 1 << 40
+    need = ctypes.c_uint64(7)
+    # every operand suits the tensor maps: no workspace
+    assert lib.gemm_workspace_bytes(big, 64, 2 * big, 64, 3 * big, 64, 64, 64, 64, ctypes.byref(need)) == g.GEMM_OK
+    assert need.value == 0
+    # A pitch 1001 -> copy with pitch 1008; B and C fine
+    assert lib.gemm_workspace_bytes(big, 1001, 2 * big, 64, 3 * big, 64, 300, 64, 1001, ctypes.byref(need)) == 0
+    assert need.value == -(-(300 * 1008 * 2) // 256) * 256
+    # all three: A 300x1008, B 1001x1000, C 300x1000, each region 256-byte aligned
+    assert lib.gemm_workspace_bytes(big + 2, 1001, 2 * big, 999, 3 * big + 6, 999, 300, 999, 1001,
+                                    ctypes.byref(need)) == 0
+    r = lambda x: -(-x // 256) * 256  # noqa: E731
+    assert need.value == r(300 * 1008 * 2) + r(1001 * 1000 * 2) + r(300 * 1000 * 2)
+    # K == 0: A and B are not read, only C may need a copy
+    assert lib.gemm_workspace_bytes(0, 0, 0, 64, 3 * big + 2, 64, 10, 64, 0, ctypes.byref(need)) == 0
+    assert need.value == r(10 * 64 * 2)
+    # validation as for the GEMM
+    assert lib.gemm_workspace_bytes(big, 10, 2 * big, 64, 3 * big, 64, 64, 64, 64,
+                                    ctypes.byref(need)) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_workspace_bytes(big, 64, 2 * big, 64, 3 * big, 64, 64, 64, 64, None) == g.GEMM_ERR_INVALID_ARG

@@ -198,8 +198,11 @@ GENERIC = [
 ]
 
 
+@pytest.mark.parametrize("repack", [False, True])
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc,oa,ob,oc", GENERIC)
-def test_generic_load_path(gemm_lib, M, N, K, lda, ldb, ldc, oa, ob, oc):
+def test_generic_load_path(gemm_lib, M, N, K, lda, ldb, ldc, oa, ob, oc, repack):
+    """repack=False: the generic-load kernel; repack=True: operands copied into
+    a workspace, the TMA kernels, C copied back."""
     A, B = inputs.gemm_inputs(M, N, K, seed=M + 5 * N + 11 * K)
     nan = float("nan")
     a_buf = torch.full((oa + M * lda,), nan, dtype=torch.float16)
@@ -213,9 +216,14 @@ def test_generic_load_path(gemm_lib, M, N, K, lda, ldb, ldc, oa, ob, oc):
     b_view = b_buf.cuda()[ob:].view(K, ldb)[:, :N]
     c_view = c_buf[pad + oc:pad + oc + M * ldc].view(torch.float16).view(M, ldc)[:, :N]
     n0 = g.launch_count()
-    g.gemm(a_view, b_view, out=c_view)       # the NaN padding of A and B is never read
+    g.gemm(a_view, b_view, out=c_view, repack=repack)   # the NaN padding of A and B is never read
     assert g.query_status() == g.GEMM_OK
-    assert g.launch_count() - n0 == 1
+    copies = 0
+    if repack:
+        copies = sum(not (t.data_ptr() % 16 == 0 and (t.stride(0) % 8 == 0 or t.shape[0] == 1))
+                     for t in (a_view, b_view, c_view))
+        assert (g.workspace_bytes(a_view, b_view, c_view) > 0) == (copies > 0)
+    assert g.launch_count() - n0 == 1 + copies
     check_against_oracle(A, B, c_view.contiguous())
     assert torch.all(c_buf[:pad + oc] == canary) and torch.all(c_buf[pad + oc + M * ldc:] == canary)
     if ldc > N:
@@ -241,12 +249,48 @@ def test_generic_path_k_zero_and_matches_tma_path(gemm_lib):
            torch.empty((0, N), dtype=torch.float16, device="cuda"), out=c_buf.view(torch.float16)[:, :N])
     assert g.query_status() == g.GEMM_OK
     assert torch.all(c_buf[:, :N] == 0) and torch.all(c_buf[:, N:] == 0x7E01)
-    # the same problem through both kernels: identical bits (same MMA order per 64-deep k step)
+    # the same problem through the three routes: identical bits (the same
+    # 128x256x64 tiles and MMA order over the same values)
     M, N, K = 384, 512, 640
     A, B = inputs.gemm_inputs(M, N, K, seed=77)
     a, b = A.cuda(), B.cuda()
     c_tma = g.gemm(a, b, tile_cfg=g.TILE_128x256x64)
     a_off = torch.empty(M * K + 1, dtype=torch.float16, device="cuda")
     a_off[1:] = a.reshape(-1)
-    c_gen = g.gemm(a_off[1:].view(M, K), b)          # A 2 bytes off a 16-byte boundary
-    assert torch.equal(c_tma, c_gen)
+    a_mis = a_off[1:].view(M, K)                     # A 2 bytes off a 16-byte boundary
+    c_gen = g.gemm(a_mis, b, repack=False)
+    c_rep = g.gemm(a_mis, b, tile_cfg=g.TILE_128x256x64, repack=True)
+    assert torch.equal(c_tma, c_gen) and torch.equal(c_tma, c_rep)
+
+
+def test_workspace_entry_point_rules(gemm_lib):
+    lib = g.load()
+    s = torch.cuda.current_stream().cuda_stream
+    M, N, K = 200, 304, 100     # only A (pitch 100, base 2 bytes off) needs a copy; its pitch becomes 104
+    A, B = inputs.gemm_inputs(M, N, K, seed=5)
+    a_off = torch.empty(M * K + 1, dtype=torch.float16, device="cuda")
+    a_off[1:] = A.cuda().reshape(-1)
+    a = a_off[1:]
+    b = B.cuda()
+    c = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    need = g.workspace_bytes(a.view(M, K), b, c)
+    assert need == -(-(M * 104 * 2) // 256) * 256
+    args = (a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, M, N, K, 8, 0, None)
+    # too small or misaligned workspace: the generic kernel runs instead (same result)
+    ws = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    n0 = g.launch_count()
+    assert lib.gemm_f16_f32acc_strided_ws(*args, ws.data_ptr(), need - 1, s) == g.GEMM_OK
+    assert lib.gemm_f16_f32acc_strided_ws(*args, ws.data_ptr() + 16, need, s) == g.GEMM_OK
+    assert g.launch_count() - n0 == 2
+    check_against_oracle(A, B, c)
+    # a workspace over an operand (here C, whose 120 KB hold the 41 KB asked for) is an argument error
+    assert c.data_ptr() % 256 == 0
+    n0 = g.launch_count()
+    assert lib.gemm_f16_f32acc_strided_ws(*args, c.data_ptr(), need, s) == g.GEMM_ERR_INVALID_ARG
+    assert g.launch_count() == n0
+    # the workspace route: one copy of A, one GEMM
+    c.zero_()
+    assert lib.gemm_f16_f32acc_strided_ws(*args, ws.data_ptr(), need, s) == g.GEMM_OK
+    assert g.launch_count() - n0 == 2
+    assert g.query_status() == g.GEMM_OK
+    check_against_oracle(A, B, c)

@@ -34,13 +34,13 @@ def test_watchdog_timeout_reports_and_recovers(gemm_lib, cfg):
     try:
         g.set_watchdog_ns(50_000_000)  # 50 ms
         g.set_fault_injection(1)
-        g.gemm(a, b, tile_cfg=cfg)
+        g.gemm(a, b, tile_cfg=cfg, repack=False)
         assert g.query_status() == g.GEMM_ERR_TIMEOUT
         assert g.query_status() == g.GEMM_OK  # the query clears the word
     finally:
         g.set_fault_injection(0)
         g.set_watchdog_ns(0)
-    C = g.gemm(a, b, tile_cfg=cfg)
+    C = g.gemm(a, b, tile_cfg=cfg, repack=False)
     assert g.query_status() == g.GEMM_OK
     check_against_oracle(A, B, C)
 
