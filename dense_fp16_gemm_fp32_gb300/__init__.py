@@ -17,11 +17,16 @@ from ._binding import (  # noqa: F401
     GEMM_OK,
     SOFTMAX_MAX_COLS,
     TILE_128x64x32,
+    TILE_128x128x64,
+    TILE_128x128x64_SPLITK,
     TILE_128x256x64,
     TILE_256x256x64_PAIR,
     TILE_256x256x128_PAIR,
     TILE_AUTO,
+    TILE_COUNT,
     GemmError,
+    autotune,
+    autotune_clear,
     gemm,
     header_functions,
     last_cuda_error,

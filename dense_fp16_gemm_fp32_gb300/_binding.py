@@ -26,6 +26,9 @@ TILE_128x256x64 = 1
 TILE_128x64x32 = 2
 TILE_256x256x64_PAIR = 3
 TILE_256x256x128_PAIR = 4
+TILE_128x128x64 = 5
+TILE_128x128x64_SPLITK = 6
+TILE_COUNT = 7
 
 DEFAULT_GROUP_SIZE_M = 8
 
@@ -72,6 +75,10 @@ _SIGNATURES = {
                                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                   ctypes.c_int32, ctypes.c_int32, _c_void_p, _c_void_p,
                                                   ctypes.c_uint64, _c_void_p]),
+    "gemm_autotune": (ctypes.c_int, [_c_void_p, ctypes.c_int64, _c_void_p, ctypes.c_int64, _c_void_p, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                     _c_void_p, _c_void_p, _c_void_p]),
+    "gemm_autotune_clear": (ctypes.c_int, []),
     "softmax_rows_f32": (ctypes.c_int, [_c_void_p, ctypes.c_int64, _c_void_p, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.c_int64, _c_void_p]),
     "softmax_rows_plan": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, _c_void_p, _c_void_p, _c_void_p]),
@@ -128,6 +135,25 @@ def _check(rc: int, what: str):
 
 def _stream_ptr(device: torch.device):
     return torch.cuda.current_stream(device).cuda_stream
+
+
+class _Nothing:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *exc):
+        return False
+
+
+_NOTHING = _Nothing()
+
+
+def _on_device(device: torch.device):
+    """torch.cuda.device(device), skipped when it is already current (the
+    switch costs microseconds per call)."""
+    if device.index is None or device.index == torch.cuda.current_device():
+        return _NOTHING
+    return torch.cuda.device(device)
 
 
 def _check_operand(t: torch.Tensor, name: str):
@@ -196,20 +222,25 @@ def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZ
         if trace.dtype != torch.int32 or trace.device != a.device or not trace.is_contiguous():
             raise ValueError("trace must be a contiguous int32 tensor on a's device")
         trace_ptr = trace.data_ptr()
-    lib = load()
-    args = (a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(), _ld(out), M, N, K)
-    with torch.cuda.device(a.device):
+    lib = _lib if _lib is not None else load()
+    pa, pb, pc = a.data_ptr(), b.data_ptr(), out.data_ptr()
+    lda, ldb, ldc = _ld(a), _ld(b), _ld(out)
+    args = (pa, lda, pb, ldb, pc, ldc, M, N, K)
+    # operands that already suit the tensor maps need no workspace query
+    tma_shaped = (pc | (pa | pb if K else 0)) & 15 == 0 and (ldc | (lda | ldb if K else 0)) & 7 == 0
+    dev = a.device
+    with _on_device(dev):
         need = ctypes.c_uint64(0)
-        if repack:
+        if repack and not tma_shaped:
             _check(lib.gemm_workspace_bytes(*args, ctypes.byref(need)), "gemm_workspace_bytes")
+        stream = torch.cuda.current_stream(dev).cuda_stream
         if need.value:
-            ws = torch.empty(need.value, dtype=torch.uint8, device=a.device)  # caching allocator: stream-ordered reuse
+            ws = torch.empty(need.value, dtype=torch.uint8, device=dev)  # caching allocator: stream-ordered reuse
             rc = lib.gemm_f16_f32acc_strided_ws(*args, int(group_size_m), int(tile_cfg), trace_ptr, ws.data_ptr(),
-                                                need.value, _stream_ptr(a.device))
+                                                need.value, stream)
             _check(rc, "gemm_f16_f32acc_strided_ws")
         else:
-            rc = lib.gemm_f16_f32acc_strided(*args, int(group_size_m), int(tile_cfg), trace_ptr,
-                                             _stream_ptr(a.device))
+            rc = lib.gemm_f16_f32acc_strided(*args, int(group_size_m), int(tile_cfg), trace_ptr, stream)
             _check(rc, "gemm_f16_f32acc_strided")
     return out
 
@@ -309,8 +340,8 @@ def softmax(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
         _check_rows(out, "out")
         if tuple(out.shape) != (M, n) or out.device != x.device:
             raise ValueError(f"out must be [{M},{n}] on {x.device}")
-    lib = load()
-    with torch.cuda.device(x.device):
+    lib = _lib if _lib is not None else load()
+    with _on_device(x.device):
         rc = lib.softmax_rows_f32(x.data_ptr(), _row_pitch(x), out.data_ptr(), _row_pitch(out), M, n,
                                   _stream_ptr(x.device))
     _check(rc, "softmax_rows_f32")
@@ -339,3 +370,28 @@ def workspace_bytes(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor) -> int:
     _check(load().gemm_workspace_bytes(a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(), _ld(out), M, N, K,
                                        ctypes.byref(need)), "gemm_workspace_bytes")
     return int(need.value)
+
+
+def autotune(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
+             group_size_m: int = DEFAULT_GROUP_SIZE_M, reps: int = 20) -> dict:
+    """Times every tile configuration on a @ b (out is overwritten) and makes
+    the fastest the TILE_AUTO choice for this shape on this device.
+    Returns {"best": cfg, "us": {cfg: microseconds per launch}}."""
+    _check_operand(a, "a")
+    _check_operand(b, "b")
+    M, K = a.shape
+    N = b.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=a.device)
+    best = ctypes.c_int32(0)
+    us = (ctypes.c_float * TILE_COUNT)()
+    with _on_device(a.device):
+        rc = load().gemm_autotune(a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(), _ld(out), M, N, K,
+                                  int(group_size_m), int(reps), ctypes.byref(best), us,
+                                  _stream_ptr(a.device))
+    _check(rc, "gemm_autotune")
+    return {"best": best.value, "us": {c: float(us[c]) for c in range(1, TILE_COUNT)}}
+
+
+def autotune_clear() -> None:
+    _check(load().gemm_autotune_clear(), "gemm_autotune_clear")

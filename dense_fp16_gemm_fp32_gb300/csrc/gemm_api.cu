@@ -8,10 +8,12 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "gemm_kernel.cuh"
 #include "gemm_kernel_pair.cuh"
+#include "gemm_kernel_splitk.cuh"
 #include "gemm_sm103.h"
 
 namespace {
@@ -20,8 +22,11 @@ using namespace gemm103;
 
 using Cfg128x256 = TileCfg<128, 256, 64, 4>;
 using Cfg128x64 = TileCfg<128, 64, 32, 6>;
+using Cfg128x128 = TileCfg<128, 128, 64, 6>;
+using CfgSplitK = TileCfg<128, 128, 64, 4>;  // the ring also holds the 64 KiB fp32 partial tile
 using CfgGeneric = TileCfg<128, 256, 64, 4, true>;  // plain loads and stores (operands TMA cannot address)
-constexpr int kGenericCfgId = 5;
+constexpr int kGenericCfgId = 7;
+constexpr int kMaxSplitK = 8;  // portable cluster size
 using CfgPair256 = PairCfg<6>;
 using CfgPair256Deep = PairCfg<3, 128>;
 
@@ -30,7 +35,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumCfgs = 6;  // the five tile configurations and the generic-load kernel
+constexpr int kNumCfgs = 8;  // the tile configurations 1..6 and the generic-load kernel
 constexpr int64_t kMaxExtent = int64_t(1) << 30;
 constexpr uint64_t kDefaultWatchdogNs = 2000000000ull;
 
@@ -172,12 +177,51 @@ bool tma_ok(const Problem& pr)
     return true;
 }
 
-// GEMM_TILE_AUTO: the CTA-pair 256x256 tile with 128-deep k steps unless the
-// problem has at most one 128-row band, where half of every pair tile would
-// be empty.
-int resolve_cfg(int32_t tile_cfg, int64_t M, int32_t* tm, int32_t* tn, int32_t* tk)
+// Tile configurations gemm_autotune chose, per device and shape.
+struct TuneKey {
+    int dev;
+    int64_t M, N, K;
+    bool operator<(const TuneKey& o) const
+    {
+        if (dev != o.dev) return dev < o.dev;
+        if (M != o.M) return M < o.M;
+        if (N != o.N) return N < o.N;
+        return K < o.K;
+    }
+};
+std::mutex g_tune_mu;
+std::map<TuneKey, int32_t> g_tuned;
+std::atomic<bool> g_any_tuned{false};
+
+int32_t tuned_cfg(int64_t M, int64_t N, int64_t K)
 {
-    if (tile_cfg == GEMM_TILE_AUTO) tile_cfg = M > 128 ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x256x64;
+    if (!g_any_tuned.load(std::memory_order_relaxed)) return GEMM_TILE_AUTO;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_TILE_AUTO;
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    const auto it = g_tuned.find(TuneKey{dev, M, N, K});
+    return it == g_tuned.end() ? GEMM_TILE_AUTO : it->second;
+}
+
+// Below this many 256 x 256 tiles, fewer than half of the 76 CTA pairs of a
+// GB300 would have work: the one-CTA 128 x 128 tile spreads the problem over
+// four times as many SMs (measured faster at 512^3, 1024x768x128, 1024^3).
+constexpr int64_t kFewPairTiles = 32;
+
+// GEMM_TILE_AUTO: the configuration gemm_autotune chose for this shape on
+// the current device, if any; else the one-CTA 128 x 256 tile when the
+// problem has at most one 128-row band (half of every pair tile would be
+// empty), the one-CTA 128 x 128 tile when it has fewer than kFewPairTiles
+// 256 x 256 tiles, and the CTA-pair 256 x 256 tile with 128-deep k steps.
+int resolve_cfg(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tm, int32_t* tn, int32_t* tk)
+{
+    if (tile_cfg == GEMM_TILE_AUTO) tile_cfg = tuned_cfg(M, N, K);
+    if (tile_cfg == GEMM_TILE_AUTO) {
+        const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+        tile_cfg = M <= 128                     ? GEMM_TILE_128x256x64
+                   : pair_tiles < kFewPairTiles ? GEMM_TILE_128x128x64
+                                                : GEMM_TILE_256x256x128_PAIR;
+    }
     switch (tile_cfg) {
         case GEMM_TILE_128x256x64:
             *tm = Cfg128x256::TM, *tn = Cfg128x256::TN, *tk = Cfg128x256::TK;
@@ -191,6 +235,12 @@ int resolve_cfg(int32_t tile_cfg, int64_t M, int32_t* tm, int32_t* tn, int32_t* 
         case GEMM_TILE_256x256x128_PAIR:
             *tm = CfgPair256Deep::TM, *tn = CfgPair256Deep::TN, *tk = CfgPair256Deep::TK;
             return GEMM_TILE_256x256x128_PAIR;
+        case GEMM_TILE_128x128x64:
+            *tm = Cfg128x128::TM, *tn = Cfg128x128::TN, *tk = Cfg128x128::TK;
+            return GEMM_TILE_128x128x64;
+        case GEMM_TILE_128x128x64_SPLITK:
+            *tm = CfgSplitK::TM, *tn = CfgSplitK::TN, *tk = CfgSplitK::TK;
+            return GEMM_TILE_128x128x64_SPLITK;
         default:
             return -1;
     }
@@ -382,6 +432,88 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     return GEMM_OK;
 }
 
+// K-split factor for 128 x 128 tiles: the largest power of two up to the
+// portable cluster size that gives every CTA at least one k step and keeps
+// tiles x S within one CTA per SM.
+int splitk_factor(int64_t tiles, int64_t k_tiles, int64_t sm_count)
+{
+    int s = 1;
+    while (s < kMaxSplitK && 2 * s <= k_tiles && tiles * 2 * s <= sm_count) s *= 2;
+    return s;
+}
+
+// One cluster of S CTAs per 128 x 128 tile, the K range split across the
+// cluster (gemm_kernel_splitk.cuh); S == 1 runs the one-CTA 128 x 128 kernel.
+int launch_splitk(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
+{
+    using Cfg = CfgSplitK;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != GEMM_OK) return rc;
+    const int64_t num_pid_m = (pr.M + Cfg::TM - 1) / Cfg::TM;
+    const int64_t num_pid_n = (pr.N + Cfg::TN - 1) / Cfg::TN;
+    const int64_t num_tiles = num_pid_m * num_pid_n;
+    const int64_t k_tiles = (pr.K + Cfg::TK - 1) / Cfg::TK;
+    const int S = splitk_factor(num_tiles, k_tiles, d->sm_count);
+    if (S == 1) return launch<Cfg128x128>(pr, GEMM_TILE_128x128x64, trace, stream);
+    auto kernel = S == 2 ? gemm_f16_f32acc_splitk_kernel<Cfg, 2>
+                : S == 4 ? gemm_f16_f32acc_splitk_kernel<Cfg, 4> : gemm_f16_f32acc_splitk_kernel<Cfg, 8>;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!d->attr_set[cfg_id]) {
+            for (auto k : {gemm_f16_f32acc_splitk_kernel<Cfg, 2>, gemm_f16_f32acc_splitk_kernel<Cfg, 4>,
+                           gemm_f16_f32acc_splitk_kernel<Cfg, 8>}) {
+                const cudaError_t e =
+                    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+            d->attr_set[cfg_id] = true;
+        }
+    }
+    CUtensorMap ma, mb;
+    rc = make_map(&ma, pr.A, pr.K, pr.M, pr.lda, Cfg::TK, Cfg::TM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != GEMM_OK) return rc;
+    rc = make_map(&mb, pr.B, pr.N, pr.K, pr.ldb, 64, Cfg::TK, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != GEMM_OK) return rc;
+
+    GemmParams p;
+    p.C = static_cast<uint16_t*>(pr.C);
+    p.ldc = pr.ldc;
+    p.M = static_cast<int32_t>(pr.M);
+    p.N = static_cast<int32_t>(pr.N);
+    p.K = static_cast<int32_t>(pr.K);
+    p.num_pid_m = static_cast<int32_t>(num_pid_m);
+    p.num_pid_n = static_cast<int32_t>(num_pid_n);
+    p.num_tiles = static_cast<int32_t>(num_tiles);
+    p.num_k_tiles = static_cast<int32_t>(k_tiles);
+    p.group_size_m = pr.group_size_m > p.num_pid_m ? p.num_pid_m : pr.group_size_m;
+    p.status = d->status;
+    p.trace = trace;
+    p.watchdog_ns = watchdog_ns();
+    p.fault_mode = g_fault_mode.load();
+    p.num_full_tiles = p.num_tiles;
+    p.num_units = p.num_tiles;
+    p.A = p.B = nullptr;
+    p.lda = p.ldb = 0;
+
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = S;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(num_tiles * S), 1, 1);
+    lc.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = stream;
+    lc.attrs = &attr;
+    lc.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, ma, mb, p);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
 }  // namespace
 
 namespace gemm103 {
@@ -503,6 +635,10 @@ int dispatch_tma(const Problem& pr, int cfg, int32_t* trace, cudaStream_t s)
             return launch_pair<CfgPair256>(pr, cfg, trace, s);
         case GEMM_TILE_256x256x128_PAIR:
             return launch_pair<CfgPair256Deep>(pr, cfg, trace, s);
+        case GEMM_TILE_128x128x64:
+            return launch<Cfg128x128>(pr, cfg, trace, s);
+        case GEMM_TILE_128x128x64_SPLITK:
+            return launch_splitk(pr, cfg, trace, s);
         default:
             return launch<Cfg128x256>(pr, cfg, trace, s);
     }
@@ -530,7 +666,7 @@ int gemm_f16_f32acc_strided_ws(const void* A, int64_t lda, const void* B, int64_
 {
     const Problem pr{A, B, C, M, N, K, group_size_m, lda, ldb, ldc};
     int32_t tm, tn, tk;
-    const int cfg = resolve_cfg(tile_cfg, M, &tm, &tn, &tk);
+    const int cfg = resolve_cfg(tile_cfg, M, N, K, &tm, &tn, &tk);
     if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
     int rc = validate(pr);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
@@ -576,7 +712,7 @@ int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t l
 {
     const Problem pr{A, B, C, M, N, K, group_size_m, lda, ldb, ldc};
     int32_t tm, tn, tk;
-    const int cfg = resolve_cfg(tile_cfg, M, &tm, &tn, &tk);
+    const int cfg = resolve_cfg(tile_cfg, M, N, K, &tm, &tn, &tk);
     if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
     int rc = validate(pr);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
@@ -597,12 +733,74 @@ int gemm_f16_f32acc(const void* A, const void* B, void* C, int64_t M, int64_t N,
     return gemm_f16_f32acc_tiled(A, B, C, M, N, K, group_size_m, GEMM_TILE_AUTO, nullptr, stream);
 }
 
+int gemm_autotune(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t M, int64_t N,
+                  int64_t K, int32_t group_size_m, int32_t reps, int32_t* best_cfg, float* us_per_cfg, void* stream)
+{
+    if (reps < 1 || reps > 10000) return GEMM_ERR_INVALID_ARG;
+    const Problem pr{A, B, C, M, N, K, group_size_m, lda, ldb, ldc};
+    int rc = validate(pr);
+    if (rc != GEMM_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_ERR_INVALID_ARG;  // nothing to time
+    if (!tma_ok(pr)) return GEMM_ERR_UNSUPPORTED;      // the tile configurations are TMA kernels
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaEvent_t ev[2];
+    e = cudaEventCreate(&ev[0]);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaEventCreate(&ev[1]);
+    if (e != cudaSuccess) {
+        cudaEventDestroy(ev[0]);
+        return cuda_fail(e);
+    }
+    int32_t best = -1;
+    float best_us = 0.f;
+    for (int32_t cfg = 1; cfg < GEMM_TILE_COUNT && rc == GEMM_OK; ++cfg) {
+        for (int i = 0; i < 2 && rc == GEMM_OK; ++i) rc = dispatch_tma(pr, cfg, nullptr, s);  // warm-up
+        if (rc != GEMM_OK) break;
+        if ((e = cudaEventRecord(ev[0], s)) != cudaSuccess) rc = cuda_fail(e);
+        for (int i = 0; i < reps && rc == GEMM_OK; ++i) rc = dispatch_tma(pr, cfg, nullptr, s);
+        if (rc != GEMM_OK) break;
+        if ((e = cudaEventRecord(ev[1], s)) != cudaSuccess || (e = cudaEventSynchronize(ev[1])) != cudaSuccess) {
+            rc = cuda_fail(e);
+            break;
+        }
+        float ms = 0.f;
+        if ((e = cudaEventElapsedTime(&ms, ev[0], ev[1])) != cudaSuccess) {
+            rc = cuda_fail(e);
+            break;
+        }
+        const float us = 1000.f * ms / static_cast<float>(reps);
+        if (us_per_cfg != nullptr) us_per_cfg[cfg] = us;
+        if (best < 0 || us < best_us) best = cfg, best_us = us;
+    }
+    cudaEventDestroy(ev[0]);
+    cudaEventDestroy(ev[1]);
+    if (rc != GEMM_OK) return rc;
+    if (us_per_cfg != nullptr) us_per_cfg[0] = best_us;
+    {
+        std::lock_guard<std::mutex> lock(g_tune_mu);
+        g_tuned[TuneKey{dev, M, N, K}] = best;
+        g_any_tuned.store(true);
+    }
+    if (best_cfg != nullptr) *best_cfg = best;
+    return GEMM_OK;
+}
+
+int gemm_autotune_clear(void)
+{
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    g_tuned.clear();
+    g_any_tuned.store(false);
+    return GEMM_OK;
+}
+
 int gemm_tile_shape(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tile_m, int32_t* tile_n,
                     int32_t* tile_k)
 {
-    (void)N, (void)K;
     int32_t tm, tn, tk;
-    if (resolve_cfg(tile_cfg, M, &tm, &tn, &tk) < 0) return GEMM_ERR_UNSUPPORTED;
+    if (resolve_cfg(tile_cfg, M, N, K, &tm, &tn, &tk) < 0) return GEMM_ERR_UNSUPPORTED;
     if (tile_m) *tile_m = tm;
     if (tile_n) *tile_n = tn;
     if (tile_k) *tile_k = tk;
@@ -612,9 +810,8 @@ int gemm_tile_shape(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* 
 int gemm_launch_plan(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* grid_ctas, int32_t* num_tiles,
                      int32_t* split_tiles)
 {
-    (void)K;
     int32_t tm, tn, tk;
-    const int cfg = resolve_cfg(tile_cfg, M, &tm, &tn, &tk);
+    const int cfg = resolve_cfg(tile_cfg, M, N, K, &tm, &tn, &tk);
     if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
     if (M < 0 || N < 0) return GEMM_ERR_INVALID_ARG;
     const int64_t tiles = ((M + tm - 1) / tm) * ((N + tn - 1) / tn);
@@ -631,6 +828,9 @@ int gemm_launch_plan(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t*
         split = split_tail_tiles(tiles, clusters);
         const int64_t units = tiles + split;
         ctas = 2 * (units < clusters ? units : clusters);
+    } else if (cfg == GEMM_TILE_128x128x64_SPLITK &&
+               splitk_factor(tiles, (K + tk - 1) / tk, d->sm_count) > 1) {
+        ctas = tiles * splitk_factor(tiles, (K + tk - 1) / tk, d->sm_count);  // one cluster per tile
     } else {
         // one-CTA kernels: occupancy is set up on first launch; report the SM bound
         const int64_t slots = static_cast<int64_t>(d->sm_count) * (d->attr_set[cfg] ? d->ctas_per_sm[cfg] : 1);

@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 acc_phase ^= 1u;
             }
         }
-        if (lane == 0) bulk_wait_group<0>();  // every store of C has completed
+        if (lane == 0) bulk_wait_group_read<0>();  // every store of C has read its staging buffer
         __syncwarp();
     }
 

@@ -198,6 +198,13 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_shared_to_rank(uint32_t saddr, uint32_t rank)
 {
@@ -221,6 +228,17 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
 {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// 16-byte load from shared memory of any CTA of the cluster (a mapa address).
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
     return v;
 }
 

@@ -65,13 +65,24 @@ typedef enum {
 
 /* Tile configurations (TILE_M x TILE_N x TILE_K). */
 typedef enum {
-    GEMM_TILE_AUTO = 0,       /* the library picks: 256x256x128_PAIR when M > 128, else 128x256x64 */
+    GEMM_TILE_AUTO = 0,       /* the library picks: the configuration gemm_autotune chose for
+                                 this (M, N, K) on the current device; else 128x256x64 when
+                                 M <= 128, 128x128x64 when the problem has fewer than 32
+                                 tiles of 256x256, and 256x256x128_PAIR otherwise */
     GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */
     GEMM_TILE_128x64x32 = 2,  /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
                                  BLOCK_SIZE_N 64, BLOCK_SIZE_K 32) */
     GEMM_TILE_256x256x64_PAIR = 3, /* a 2-CTA cluster per tile (tcgen05 cta_group::2): each
                                  CTA stages 128 rows of A and 128 columns of B, 6 stages */
-    GEMM_TILE_256x256x128_PAIR = 4 /* as 3 with 128-deep k steps, 3 stages */
+    GEMM_TILE_256x256x128_PAIR = 4, /* as 3 with 128-deep k steps, 3 stages */
+    GEMM_TILE_128x128x64 = 5, /* 1 CTA per tile, 6 stages: twice the tiles of 128x256 for
+                                 problems with few tiles */
+    GEMM_TILE_128x128x64_SPLITK = 6, /* a cluster of S = 2, 4 or 8 CTAs per 128x128 tile, each
+                                 running 1/S of the k steps; the fp32 partials are summed
+                                 through distributed shared memory (S: the largest power of
+                                 two <= 8 with S <= ceil(K/64) and tiles * S <= SMs; S = 1
+                                 runs the 128x128x64 kernel) */
+    GEMM_TILE_COUNT = 7       /* number of values above, GEMM_TILE_AUTO included */
 } gemm_tile_cfg_t;
 
 /*
@@ -135,6 +146,31 @@ int gemm_f16_f32acc_tiled(const void* A, const void* B, void* C, int64_t M, int6
 int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t M,
                             int64_t N, int64_t K, int32_t group_size_m, int32_t tile_cfg, int32_t* tile_trace,
                             void* stream);
+
+/*
+ * Times every tile configuration (1 .. GEMM_TILE_COUNT-1) on these operands
+ * and remembers the fastest for (M, N, K) on the current device, so that
+ * GEMM_TILE_AUTO (and gemm_tile_shape / gemm_launch_plan for it) uses it from
+ * then on. The analogue of the tutorial kernel's autotuning over a list of
+ * configurations keyed on the problem shape.
+ *
+ *   A, lda, B, ldb, C, ldc, M, N, K, group_size_m
+ *              as for gemm_f16_f32acc_strided; C is overwritten (it holds
+ *              A*B afterwards). The operands must suit the TMA kernels
+ *              (16-byte aligned bases, pitches multiples of 8), else
+ *              GEMM_ERR_UNSUPPORTED; M == 0 or N == 0 -> GEMM_ERR_INVALID_ARG.
+ *   reps       timed launches per configuration, 1..10000 (after 2 warm-up
+ *              launches), timed with CUDA events on `stream`
+ *   best_cfg   host int32, or NULL: the chosen configuration
+ *   us_per_cfg host array of GEMM_TILE_COUNT floats, or NULL: [c] = mean
+ *              microseconds per launch of configuration c, [0] = the best
+ *
+ * Synchronous (waits for its events): not for use under stream capture.
+ * gemm_autotune_clear() forgets every choice.
+ */
+int gemm_autotune(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t M, int64_t N,
+                  int64_t K, int32_t group_size_m, int32_t reps, int32_t* best_cfg, float* us_per_cfg, void* stream);
+int gemm_autotune_clear(void);
 
 /*
  * Bytes of workspace gemm_f16_f32acc_strided_ws needs to run these operands

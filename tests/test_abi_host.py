@@ -40,11 +40,15 @@ def test_status_strings(lib):
 
 def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_AUTO, M=128) == (128, 256, 64)
-    assert g.tile_shape(g.TILE_AUTO, M=129) == (256, 256, 128)
+    assert g.tile_shape(g.TILE_AUTO, M=129, N=8192) == (256, 256, 128)   # 32 pair tiles
+    assert g.tile_shape(g.TILE_AUTO, M=512, N=512) == (128, 128, 64)      # 4 pair tiles: few
+    assert g.tile_shape(g.TILE_AUTO, M=8192, N=8192, K=8192) == (256, 256, 128)
     assert g.tile_shape(g.TILE_256x256x64_PAIR) == (256, 256, 64)
     assert g.tile_shape(g.TILE_256x256x128_PAIR) == (256, 256, 128)
     assert g.tile_shape(g.TILE_128x256x64) == (128, 256, 64)
     assert g.tile_shape(g.TILE_128x64x32) == (128, 64, 32)
+    assert g.tile_shape(g.TILE_128x128x64) == (128, 128, 64)
+    assert g.tile_shape(g.TILE_128x128x64_SPLITK) == (128, 128, 64)
     with pytest.raises(g.GemmError) as e:
         g.tile_shape(17)
     assert e.value.code == g.GEMM_ERR_UNSUPPORTED
@@ -195,3 +199,15 @@ def test_workspace_bytes_without_gpu(lib):
     assert lib.gemm_workspace_bytes(big, 10, 2 * big, 64, 3 * big, 64, 64, 64, 64,
                                     ctypes.byref(need)) == g.GEMM_ERR_INVALID_ARG
     assert lib.gemm_workspace_bytes(big, 64, 2 * big, 64, 3 * big, 64, 64, 64, 64, None) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_autotune_validation_without_gpu(lib):
+    big = 1 << 40
+    args = (big, 64, 2 * big, 64, 3 * big, 64)
+    assert lib.gemm_autotune(*args, 64, 64, 64, 8, 0, None, None, None) == g.GEMM_ERR_INVALID_ARG   # reps
+    assert lib.gemm_autotune(*args, 64, 64, 64, 8, 10001, None, None, None) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_autotune(*args, 0, 64, 64, 8, 5, None, None, None) == g.GEMM_ERR_INVALID_ARG     # nothing to time
+    assert lib.gemm_autotune(*args, -1, 64, 64, 8, 5, None, None, None) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_autotune(big, 61, 2 * big, 64, 3 * big, 64, 64, 64, 61, 8, 5, None, None,
+                             None) == g.GEMM_ERR_UNSUPPORTED                                          # not TMA-shaped
+    assert lib.gemm_autotune_clear() == g.GEMM_OK

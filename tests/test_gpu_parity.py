@@ -16,7 +16,8 @@ from _gpu_util import check_against_oracle
 
 pytestmark = pytest.mark.gpu
 
-ALL_CFGS = [g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR]
+ALL_CFGS = [g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR,
+            g.TILE_128x128x64, g.TILE_128x128x64_SPLITK]
 
 
 @pytest.mark.parametrize("w", inputs.WORKLOADS, ids=lambda w: w.name)
@@ -32,7 +33,8 @@ def test_workload_parity(gemm_lib, w):
 
 
 @pytest.mark.parametrize("w", [w for w in inputs.WORKLOADS if w.tile_cfg == 0], ids=lambda w: w.name)
-@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR])
+@pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR,
+                                 g.TILE_128x128x64, g.TILE_128x128x64_SPLITK])
 def test_workload_parity_each_large_tile(gemm_lib, w, cfg):
     A, B = inputs.gemm_inputs(w.M, w.N, w.K, w.seed)
     C = g.gemm(A.cuda(), B.cuda(), group_size_m=w.group_size_m, tile_cfg=cfg)
@@ -294,3 +296,46 @@ def test_workspace_entry_point_rules(gemm_lib):
     assert g.launch_count() - n0 == 2
     assert g.query_status() == g.GEMM_OK
     check_against_oracle(A, B, c)
+
+
+def test_autotune_picks_fastest_and_auto_follows(gemm_lib):
+    M, N, K = 1024, 768, 256
+    A, B = inputs.gemm_inputs(M, N, K, seed=13)
+    a, b = A.cuda(), B.cuda()
+    default_shape = g.tile_shape(g.TILE_AUTO, M, N, K)
+    try:
+        r = g.autotune(a, b, reps=5)
+        assert set(r["us"]) == set(range(1, g.TILE_COUNT))
+        assert all(v > 0 for v in r["us"].values())
+        assert r["best"] == min(r["us"], key=r["us"].get)
+        # TILE_AUTO now resolves to the tuned configuration for this shape only
+        assert g.tile_shape(g.TILE_AUTO, M, N, K) == g.tile_shape(r["best"])
+        assert g.tile_shape(g.TILE_AUTO, 8192, 8192, K) == (256, 256, 128)   # other shapes: the default rule
+        n0 = g.launch_count()
+        C = g.gemm(a, b)
+        assert g.launch_count() - n0 == 1 and g.query_status() == g.GEMM_OK
+        check_against_oracle(A, B, C)
+    finally:
+        g.autotune_clear()
+    assert g.tile_shape(g.TILE_AUTO, M, N, K) == default_shape
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (512, 512, 512),      # 16 tiles x 8-way split
+    (1024, 768, 128),     # 2 k steps: 2-way
+    (300, 257, 320),      # 5 k steps over a 4-CTA cluster: the last CTA has none (a zero partial)
+    (129, 1000, 4000),    # ragged M and N, long K
+    (1, 8, 8),
+    (100, 100, 64),       # a single k step: no split
+])
+def test_split_k_cluster(gemm_lib, M, N, K):
+    A, B = inputs.gemm_inputs(M, N, K, seed=3 * M + N + K)
+    plan = g.launch_plan(M, N, K, tile_cfg=g.TILE_128x128x64_SPLITK)
+    tiles = -(-M // 128) * -(-N // 128)
+    assert plan["num_tiles"] == tiles
+    assert plan["grid_ctas"] % tiles == 0 or plan["grid_ctas"] <= tiles
+    C = g.gemm(A.cuda(), B.cuda(), tile_cfg=g.TILE_128x128x64_SPLITK)
+    assert g.query_status() == g.GEMM_OK
+    check_against_oracle(A, B, C)
+    C2 = g.gemm(A.cuda(), B.cuda(), tile_cfg=g.TILE_128x128x64_SPLITK)
+    assert torch.equal(C, C2)   # the partials are summed in a fixed order

@@ -62,6 +62,8 @@ def _kernel_trace(M, N, K, G, cfg, seed):
     (512, 1024, 256, 2, g.TILE_256x256x128_PAIR),    # 8 tiles: every tile split
     (2048, 4096, 256, 3, g.TILE_256x256x128_PAIR),
     (896, 192, 64, 2, g.TILE_128x64x32),
+    (4095, 3000, 200, 4, g.TILE_128x128x64),
+    (512, 640, 512, 2, g.TILE_128x128x64_SPLITK),   # 20 tiles, one cluster each
 ])
 def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
     A, B, C, tr, TM, TN = _kernel_trace(M, N, K, G, cfg, seed=31)
