@@ -112,6 +112,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const int lane = static_cast<int>(threadIdx.x & 31);
 
     if (threadIdx.x == 0) {
+        if (p.num_k_tiles > 0 && !Cfg::kGeneric) {  // first: the descriptors' fetch overlaps the set-up
+            tma_prefetch_desc(&tmap_a);
+            tma_prefetch_desc(&tmap_b);
+            tma_prefetch_desc(&tmap_c);
+        }
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(&full[s], Cfg::FULL_ARRIVALS);
             mbar_init(&empty[s], 1);
@@ -123,11 +128,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         mbar_init(drain, 1);
         *abort_flag = 0u;
         fence_mbar_init();
-        if (p.num_k_tiles > 0 && !Cfg::kGeneric) {
-            tma_prefetch_desc(&tmap_a);
-            tma_prefetch_desc(&tmap_b);
-            tma_prefetch_desc(&tmap_c);
-        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);

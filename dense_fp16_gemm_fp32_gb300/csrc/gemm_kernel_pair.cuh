@@ -131,6 +131,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const int32_t num_pairs = static_cast<int32_t>(gridDim.x >> 1);
 
     if (threadIdx.x == 0) {
+        if (p.num_k_tiles > 0) {  // first: the descriptors' fetch overlaps the set-up
+            tma_prefetch_desc(&tmap_a);
+            tma_prefetch_desc(&tmap_b);
+            tma_prefetch_desc(&tmap_c);
+        }
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(&full[s], 1);   // even CTA: one arrive (with the pair's byte count)
             mbar_init(&empty[s], 1);  // one commit from the MMA thread
@@ -142,11 +147,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         mbar_init(drain, 1);
         *abort_flag = 0u;
         fence_mbar_init();
-        if (p.num_k_tiles > 0) {
-            tma_prefetch_desc(&tmap_a);
-            tma_prefetch_desc(&tmap_b);
-            tma_prefetch_desc(&tmap_c);
-        }
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);

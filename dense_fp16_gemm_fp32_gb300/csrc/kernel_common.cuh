@@ -136,7 +136,9 @@ constexpr int kEpiWarpStagingBytes = 2 * kEpiBufBytes;
 // 8) is written with masked direct stores instead, leaving C's padding
 // columns untouched. Only lane 0 issues TMA stores, so lane 0 alone waits on
 // the bulk groups. kDirect: every block is written with direct stores (C's
-// base or pitch is not one a TMA store can address).
+// base or pitch is not one a TMA store can address). Direct stores are the
+// slower form even where nothing overlaps the epilogue (measured: each lane
+// owns a row, so a warp's 16-byte stores touch 32 cache lines at once).
 template <int TN, bool kDirect = false, class Release>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* staging, const CUtensorMap* tmap_c,
                                                    int32_t c_row0, int32_t n0, int32_t M, int32_t N,
@@ -155,13 +157,19 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
 #pragma unroll
         for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r[2 * i], r[2 * i + 1]);
         const int32_t x = n0 + c * kEpiChunkCols;
-        if (kDirect || ((N & 7) != 0 && x + kEpiChunkCols > N)) {  // right edge inside a 16-byte granule
+        if (kDirect || ((N & 7) != 0 && x + kEpiChunkCols > N)) {  // or right edge inside a 16-byte granule
             const int32_t row = c_row0 + lane;
             if (row < M && x < N) {
                 uint16_t* dst = C + static_cast<int64_t>(row) * ldc + x;
+                if (x + kEpiChunkCols <= N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
 #pragma unroll
-                for (int e = 0; e < kEpiChunkCols; ++e) {
-                    if (x + e < N) dst[e] = static_cast<uint16_t>(e & 1 ? (h[e >> 1] >> 16) : (h[e >> 1] & 0xFFFFu));
+                    for (int j = 0; j < 4; ++j)
+                        reinterpret_cast<uint4*>(dst)[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kEpiChunkCols; ++e) {
+                        if (x + e < N) dst[e] = static_cast<uint16_t>(e & 1 ? (h[e >> 1] >> 16) : (h[e >> 1] & 0xFFFFu));
+                    }
                 }
             }
             continue;
