@@ -276,8 +276,10 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
     std::memset(&mc, 0, sizeof(mc));
-    // C: 32 x 32 store boxes, 64-byte swizzle (matches the epilogue staging layout)
-    if (!Cfg::kGeneric) rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    // C: EPI_COLS x 32-row store boxes with the epilogue staging's swizzle
+    if (!Cfg::kGeneric)
+        rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, Cfg::EPI_COLS, 32,
+                      Cfg::EPI_COLS == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc != GEMM_OK) return rc;
     if (pr.K > 0 && !Cfg::kGeneric) {
         const CUtensorMapSwizzle a_swz = Cfg::TK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -387,8 +389,9 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     CUtensorMap ma, mb, mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
-    // C: 32 x 32 store boxes, 64-byte swizzle (matches the epilogue staging layout)
-    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    // C: EPI_COLS x 32-row store boxes with the epilogue staging's swizzle
+    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, Cfg::EPI_COLS, 32,
+                  Cfg::EPI_COLS == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc != GEMM_OK) return rc;
     if (pr.K > 0) {
         rc = make_map(&ma, pr.A, pr.K, pr.M, pr.lda, 64, Cfg::CTA_M, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -933,7 +936,8 @@ int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, in
     CUtensorMap ma, mb, mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
-    rc = make_map(&mc, C, N, M, N, kEpiChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    rc = make_map(&mc, C, N, M, N, Cfg::EPI_COLS, 32,
+                  Cfg::EPI_COLS == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc != GEMM_OK) return rc;
     if (K > 0) {
         rc = make_map(&ma, A, K, M, K, Cfg::TK, Cfg::TM, CU_TENSOR_MAP_SWIZZLE_128B);

@@ -82,7 +82,8 @@ struct TileCfg {
                                         : (2 * TN <= 256) ? 256 : 512;
 
     static constexpr int EPI_WARPS = EPI_THREADS / 32;
-    static constexpr int STAGING_BYTES = EPI_WARPS * kEpiWarpStagingBytes;
+    static constexpr int EPI_COLS = TN >= 64 ? 64 : 32;  // columns per epilogue store block
+    static constexpr int STAGING_BYTES = EPI_WARPS * EpiStaging<EPI_COLS>::WARP_BYTES;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 8;
     static constexpr int SMEM_BYTES =
         1024 /*alignment slack*/ + STAGES * (A_STAGE + B_STAGE) + STAGING_BYTES + BAR_BYTES;
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // swizzled tiles need 1024 B alignment
     uint8_t* sA = smem;
     uint8_t* sB = sA + Cfg::STAGES * Cfg::A_STAGE;
-    uint8_t* sC = sB + Cfg::STAGES * Cfg::B_STAGE;  // epilogue staging, kEpiWarpStagingBytes per warp
+    uint8_t* sC = sB + Cfg::STAGES * Cfg::B_STAGE;  // epilogue staging, one EpiStaging per epilogue warp
     uint64_t* full = reinterpret_cast<uint64_t*>(sC + Cfg::STAGING_BYTES);
     uint64_t* empty = full + Cfg::STAGES;
     uint64_t* acc_full = empty + Cfg::STAGES;
@@ -287,7 +288,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::TN);
             uint64_t* release_bar = &acc_empty[buf];
-            epilogue_tma_store<Cfg::TN, Cfg::kGeneric>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c,
+            epilogue_tma_store<Cfg::TN, Cfg::EPI_COLS, Cfg::kGeneric>(t_row, sC + (warp - 2) * EpiStaging<Cfg::EPI_COLS>::WARP_BYTES, &tmap_c,
                                         tc.pid_m * Cfg::TM + q * 32, n0, p.M, p.N, p.C, p.ldc, lane, [&]() {
                                             tc_fence_before_sync();
                                             __syncwarp();

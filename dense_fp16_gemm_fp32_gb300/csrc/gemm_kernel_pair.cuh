@@ -74,7 +74,8 @@ struct PairCfg {
     static constexpr uint32_t ACC_COLS = TN;      // one accumulator: 128 lanes x 256 fp32 columns per CTA
     static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 
-    static constexpr int STAGING_BYTES = EPI_WARPS * kEpiWarpStagingBytes;
+    static constexpr int EPI_COLS = 32;  // columns per epilogue store block (measured best for many tiles per pair)
+    static constexpr int STAGING_BYTES = EPI_WARPS * EpiStaging<EPI_COLS>::WARP_BYTES;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 8;
     static constexpr int SMEM_BYTES = 1024 + STAGES * (A_STAGE + B_STAGE) + STAGING_BYTES + BAR_BYTES;
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* sA = smem;
     uint8_t* sB = sA + Cfg::STAGES * Cfg::A_STAGE;
-    uint8_t* sC = sB + Cfg::STAGES * Cfg::B_STAGE;  // epilogue staging, kEpiWarpStagingBytes per warp
+    uint8_t* sC = sB + Cfg::STAGES * Cfg::B_STAGE;  // epilogue staging, one EpiStaging per epilogue warp
     uint64_t* full = reinterpret_cast<uint64_t*>(sC + Cfg::STAGING_BYTES);
     uint64_t* empty = full + Cfg::STAGES;
     uint64_t* acc_full = empty + Cfg::STAGES;
@@ -319,10 +320,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             };
             const int32_t c_row0 = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + q * 32;
             if (un.half < 0)
-                epilogue_tma_store<Cfg::TN>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c, c_row0, n0, p.M,
+                epilogue_tma_store<Cfg::TN, Cfg::EPI_COLS>(t_row, sC + (warp - 2) * EpiStaging<Cfg::EPI_COLS>::WARP_BYTES, &tmap_c, c_row0, n0, p.M,
                                             p.N, p.C, p.ldc, lane, release);
             else
-                epilogue_tma_store<Cfg::TN / 2>(t_row, sC + (warp - 2) * kEpiWarpStagingBytes, &tmap_c, c_row0, n0,
+                epilogue_tma_store<Cfg::TN / 2, Cfg::EPI_COLS>(t_row, sC + (warp - 2) * EpiStaging<Cfg::EPI_COLS>::WARP_BYTES, &tmap_c, c_row0, n0,
                                                 p.M, p.N, p.C, p.ldc, lane, release);
             if (++buf == 2) {
                 buf = 0;

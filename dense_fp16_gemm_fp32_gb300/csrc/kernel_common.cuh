@@ -115,17 +115,27 @@ __device__ __forceinline__ uint32_t pack_half2_rn(uint32_t lo_bits, uint32_t hi_
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Epilogue staging: each epilogue warp owns two 32-row x 32-column fp16
-// buffers (2 KiB each) laid out with the TMA 64-byte swizzle (16-byte chunk j
-// of row r sits at chunk j ^ ((r >> 1) & 3)), so the 32 lanes' 16-byte
-// shared stores are conflict free and the TMA store reads them unswizzled.
-constexpr int kEpiChunkCols = 32;
-constexpr int kEpiBufBytes = 32 * kEpiChunkCols * 2;
-constexpr int kEpiWarpStagingBytes = 2 * kEpiBufBytes;
+// Epilogue staging: each epilogue warp owns two 32-row x COLS-column fp16
+// buffers laid out with the TMA swizzle of their row length (COLS = 64: 128-
+// byte rows, 16-byte chunk j of row r at chunk j ^ (r & 7); COLS = 32: 64-byte
+// rows, chunk j ^ ((r >> 1) & 3)), so the 32 lanes' 16-byte shared stores are
+// conflict free and the TMA store reads them unswizzled. Wider blocks mean one
+// proxy fence and one TMA store per 64 columns instead of per 32 (the fence and
+// the store issue cost about as much per block as the tensor-memory load and
+// the conversion together): measured faster where the epilogue is exposed
+// (few tiles per CTA), about 0.7 % slower at 8192^3 where it always overlaps
+// the main loop; each configuration picks its width.
+template <int COLS>
+struct EpiStaging {
+    static_assert(COLS == 32 || COLS == 64, "64- or 128-byte staging rows");
+    static constexpr int BUF_BYTES = 32 * COLS * 2;
+    static constexpr int WARP_BYTES = 2 * BUF_BYTES;
+    static constexpr int CHUNKS = COLS / 8;  // 16-byte chunks per row
+};
 
 // Drains one fp32 accumulator held in tensor memory to C through TMA stores.
 //   t_row     tensor-memory address of (this warp's first lane, first column)
-//   staging   this warp's 2 x 2 KiB staging buffers (1024-byte aligned)
+//   staging   this warp's 2 staging buffers (EpiStaging<COLS>, 1024-byte aligned)
 //   c_row0    first C row of this warp's 32 rows; n0 first C column of the tile
 //   M, N, C, ldc  extents, base and row pitch of C
 //   release   called by every lane once all tensor-memory reads are done
@@ -139,52 +149,64 @@ constexpr int kEpiWarpStagingBytes = 2 * kEpiBufBytes;
 // base or pitch is not one a TMA store can address). Direct stores are the
 // slower form even where nothing overlaps the epilogue (measured: each lane
 // owns a row, so a warp's 16-byte stores touch 32 cache lines at once).
-template <int TN, bool kDirect = false, class Release>
+template <int TN, int COLS, bool kDirect = false, class Release>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* staging, const CUtensorMap* tmap_c,
                                                    int32_t c_row0, int32_t n0, int32_t M, int32_t N,
                                                    uint16_t* C, int64_t ldc, int lane, Release release)
 {
+    using St = EpiStaging<COLS>;
+    static_assert(TN % COLS == 0, "whole blocks");
     const uint32_t stage0 = smem_addr(staging);
-    const uint32_t row_off = static_cast<uint32_t>(lane) * 64u;
-    const uint32_t swz = static_cast<uint32_t>((lane >> 1) & 3);
+    const uint32_t row_off = static_cast<uint32_t>(lane) * (COLS * 2);
+    const uint32_t swz = COLS == 64 ? static_cast<uint32_t>(lane & 7) : static_cast<uint32_t>((lane >> 1) & 3);
 #pragma unroll 1
-    for (int c = 0; c < TN / kEpiChunkCols; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * kEpiChunkCols), r);
-        tmem_ld_wait();
-        if (c == TN / kEpiChunkCols - 1) release();
-        uint32_t h[16];
+    for (int c = 0; c < TN / COLS; ++c) {
+        uint32_t h[COLS / 2];
+        {
+            uint32_t r0[32];
+            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * COLS), r0);
+            if constexpr (COLS == 64) {
+                uint32_t r1[32];
+                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * COLS + 32), r1);
+                tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r[2 * i], r[2 * i + 1]);
-        const int32_t x = n0 + c * kEpiChunkCols;
-        if (kDirect || ((N & 7) != 0 && x + kEpiChunkCols > N)) {  // or right edge inside a 16-byte granule
+                for (int i = 0; i < 16; ++i) h[16 + i] = pack_half2_rn(r1[2 * i], r1[2 * i + 1]);
+            } else {
+                tmem_ld_wait();
+            }
+            if (c == TN / COLS - 1) release();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r0[2 * i], r0[2 * i + 1]);
+        }
+        const int32_t x = n0 + c * COLS;
+        if (kDirect || ((N & 7) != 0 && x + COLS > N)) {  // or right edge inside a 16-byte granule
             const int32_t row = c_row0 + lane;
             if (row < M && x < N) {
                 uint16_t* dst = C + static_cast<int64_t>(row) * ldc + x;
-                if (x + kEpiChunkCols <= N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+                if (x + COLS <= N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
+                    for (int j = 0; j < St::CHUNKS; ++j)
                         reinterpret_cast<uint4*>(dst)[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < kEpiChunkCols; ++e) {
+                    for (int e = 0; e < COLS; ++e) {
                         if (x + e < N) dst[e] = static_cast<uint16_t>(e & 1 ? (h[e >> 1] >> 16) : (h[e >> 1] & 0xFFFFu));
                     }
                 }
             }
             continue;
         }
-        const uint32_t buf = stage0 + static_cast<uint32_t>((c & 1) * kEpiBufBytes);
+        const uint32_t buf = stage0 + static_cast<uint32_t>((c & 1) * St::BUF_BYTES);
         if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
         __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < St::CHUNKS; ++j)
             st_shared_v4(buf + row_off + ((static_cast<uint32_t>(j) ^ swz) << 4), h[4 * j], h[4 * j + 1], h[4 * j + 2],
                          h[4 * j + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if (c_row0 < M && x < N) tma_store_2d(tmap_c, staging + (c & 1) * kEpiBufBytes, x, c_row0);
+            if (c_row0 < M && x < N) tma_store_2d(tmap_c, staging + (c & 1) * St::BUF_BYTES, x, c_row0);
             bulk_commit_group();  // an empty group keeps the per-buffer accounting uniform
         }
     }
