@@ -112,12 +112,17 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31);
 
-    if (threadIdx.x == 0) {
-        if (p.num_k_tiles > 0 && !Cfg::kGeneric) {  // first: the descriptors' fetch overlaps the set-up
-            tma_prefetch_desc(&tmap_a);
-            tma_prefetch_desc(&tmap_b);
-            tma_prefetch_desc(&tmap_c);
-        }
+    // Warp 0 works out its first tile (the grouped map's divisions take a few
+    // hundred cycles) while warp 2 initialises the barriers and warp 1
+    // allocates tensor memory.
+    if (threadIdx.x == 0 && p.num_k_tiles > 0 && !Cfg::kGeneric) {
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+        tma_prefetch_desc(&tmap_c);
+    }
+    TileCoord first_tc{0, 0};
+    if (warp == 0) first_tc = grouped_tile(static_cast<int32_t>(blockIdx.x), p.num_pid_m, p.num_pid_n, p.group_size_m);
+    if (threadIdx.x == 64) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(&full[s], Cfg::FULL_ARRIVALS);
             mbar_init(&empty[s], 1);
@@ -176,7 +181,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             uint32_t issued = 0, issued_parity = 0;  // per stage: ever issued / parity of the last issue
             bool ok = true;
             for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
+                const TileCoord tc = tile == static_cast<int32_t>(blockIdx.x)
+                                         ? first_tc
+                                         : grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
                 const int32_t m0 = tc.pid_m * Cfg::TM;
                 const int32_t n0 = tc.pid_n * Cfg::TN;
                 for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {

@@ -131,12 +131,17 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const int32_t pair = static_cast<int32_t>(blockIdx.x >> 1);
     const int32_t num_pairs = static_cast<int32_t>(gridDim.x >> 1);
 
-    if (threadIdx.x == 0) {
-        if (p.num_k_tiles > 0) {  // first: the descriptors' fetch overlaps the set-up
-            tma_prefetch_desc(&tmap_a);
-            tma_prefetch_desc(&tmap_b);
-            tma_prefetch_desc(&tmap_c);
-        }
+    // Warp 0 works out its first unit (the grouped map's divisions take a few
+    // hundred cycles) while warp 2 initialises the barriers and warp 1
+    // allocates tensor memory.
+    if (threadIdx.x == 0 && p.num_k_tiles > 0) {
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+        tma_prefetch_desc(&tmap_c);
+    }
+    PairUnit first_un{};
+    if (warp == 0) first_un = pair_unit(pair, p);
+    if (threadIdx.x == 64) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(&full[s], 1);   // even CTA: one arrive (with the pair's byte count)
             mbar_init(&empty[s], 1);  // one commit from the MMA thread
@@ -170,7 +175,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int32_t u = pair; ok && u < p.num_units; u += num_pairs) {
-                const PairUnit un = pair_unit(u, p);
+                const PairUnit un = u == pair ? first_un : pair_unit(u, p);
                 const int32_t m0 = un.tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M;
                 // whole tile: this CTA's 128 of 256 columns; half tile: its 64 of the half's 128
                 const int32_t n0 = un.half < 0 ? un.tc.pid_n * Cfg::TN + static_cast<int32_t>(rank) * Cfg::CTA_N
