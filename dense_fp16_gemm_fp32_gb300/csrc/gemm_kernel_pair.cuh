@@ -225,10 +225,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             bool ok = true;
             const uint32_t a_base = smem_addr(sA);
             const uint32_t b_base = smem_addr(sB);
-            const uint32_t empty0_even = map_shared_to_rank(smem_addr(&empty[0]), 0);
-            const uint32_t empty0_odd = map_shared_to_rank(smem_addr(&empty[0]), 1);
-            const uint32_t accf0_even = map_shared_to_rank(smem_addr(&acc_full[0]), 0);
-            const uint32_t accf0_odd = map_shared_to_rank(smem_addr(&acc_full[0]), 1);
             for (int32_t u = pair; ok && u < p.num_units; u += num_pairs) {
                 const uint32_t idesc = u < p.num_full_tiles ? Cfg::IDESC : Cfg::IDESC_HALF;
                 ok = warp_wait_phase<true>(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma);
@@ -248,13 +244,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                                                 kSwizzle128B);
                         bd[kk] = make_smem_desc(b_s + kk * Cfg::B_KSTEP, Cfg::B_LBO, Cfg::B_SBO, kSwizzle128B);
                     }
-                    const uint32_t off = 8u * static_cast<uint32_t>(stage);
                     if (lane == 0) {
 #pragma unroll
                         for (int kk = 0; kk < Cfg::TK / 16; ++kk)
                             tc_mma_f16_ss_pair(d_tmem, ad[kk], bd[kk], idesc, (kt > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit_pair(empty0_even + off);  // the stage is free in both CTAs
-                        tc_commit_pair(empty0_odd + off);
+                        tc_commit_pair_multicast(smem_addr(&empty[stage]), 0x3);  // the stage is free in both CTAs
                     }
                     __syncwarp();
                     if (++stage == Cfg::STAGES) {
@@ -263,10 +257,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                if (lane == 0) {
-                    tc_commit_pair(accf0_even + 8u * static_cast<uint32_t>(buf));  // accumulator complete
-                    tc_commit_pair(accf0_odd + 8u * static_cast<uint32_t>(buf));
-                }
+                if (lane == 0) tc_commit_pair_multicast(smem_addr(&acc_full[buf]), 0x3);  // accumulator complete
                 __syncwarp();
                 if (++buf == 2) {
                     buf = 0;

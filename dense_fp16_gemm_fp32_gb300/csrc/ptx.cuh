@@ -315,6 +315,17 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar_cluster_addr)
                  : "memory");
 }
 
+// One arrive on the mbarrier at shared-memory offset `bar` (this CTA's address
+// of it) in every CTA of `cta_mask`, once every pair MMA this thread issued
+// before has completed: one instruction for both CTAs of the pair.
+__device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor of tcgen05.mma (64 bits):
 //   [0,14)  start address >> 4       [16,30) leading-dimension byte offset >> 4
