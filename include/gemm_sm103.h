@@ -68,7 +68,8 @@ typedef enum {
     GEMM_TILE_AUTO = 0,       /* the library picks: the configuration gemm_autotune chose for
                                  this (M, N, K) on the current device; else 128x256x64 when
                                  M <= 128, 128x128x64 when the problem has fewer than 32
-                                 tiles of 256x256, and 256x256x128_PAIR otherwise */
+                                 tiles of 256x256, 128x256x64 when it has fewer than 76 (less
+                                 than one wave of CTA pairs), and 256x256x128_PAIR otherwise */
     GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */
     GEMM_TILE_128x64x32 = 2,  /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
                                  BLOCK_SIZE_N 64, BLOCK_SIZE_K 32) */

@@ -40,7 +40,9 @@ def test_status_strings(lib):
 
 def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_AUTO, M=128) == (128, 256, 64)
-    assert g.tile_shape(g.TILE_AUTO, M=129, N=8192) == (256, 256, 128)   # 32 pair tiles
+    assert g.tile_shape(g.TILE_AUTO, M=129, N=8192) == (128, 256, 64)    # 32 pair tiles: under one wave
+    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2048) == (128, 256, 64)   # 64 pair tiles
+    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560) == (256, 256, 128)  # 80 pair tiles
     assert g.tile_shape(g.TILE_AUTO, M=512, N=512) == (128, 128, 64)      # 4 pair tiles: few
     assert g.tile_shape(g.TILE_AUTO, M=8192, N=8192, K=8192) == (256, 256, 128)
     assert g.tile_shape(g.TILE_256x256x64_PAIR) == (256, 256, 64)
