@@ -24,11 +24,12 @@
 //                    from the swizzled shared-memory tiles, and commits each
 //                    stage back to its empty barrier and each finished tile to
 //                    an accumulator-full barrier.
-//   warps 2..5       epilogue: tcgen05.ld of 32 accumulator columns at a time
+//   warps 2..5       epilogue: tcgen05.ld of 64 accumulator columns at a time
 //                    (warp w reads TMEM lanes 32*(w%4)..+31, i.e. tile rows),
 //                    one round-to-nearest-even conversion to fp16, a swizzled
 //                    shared-memory staging buffer and a TMA store of each
-//                    32 x 32 block (the TMA unit clips rows and columns past C).
+//                    32-row x 64-column block (the TMA unit clips rows and
+//                    columns past C).
 //                    The accumulator is double buffered, so tile i's epilogue
 //                    runs under tile i+1's main loop.
 // Every mbarrier wait is bounded by %globaltimer; on expiry the CTA records a

@@ -10,17 +10,18 @@
 //     of the tile's A panel and columns [128r, 128r + 128) of its B panel into
 //     its own shared memory; the MMA reads A from each CTA's memory for that
 //     CTA's half of the rows and B from both, so each SM stages 32 KiB per
-//     k step for the same 128 x 256 x 64 of work that costs 48 KiB alone.
+//     64 k-values for the same 128 x 256 x 64 of work that costs 48 KiB alone.
 //   * Both CTAs' TMA loads complete on the even CTA's full barrier, which the
 //     even CTA arms with the pair's total byte count.
-//   * The even CTA's MMA warp runs the schedule; its lane 0 issues the MMAs and commits each stage to the
-//     empty barriers of both CTAs and each finished accumulator to the
-//     accumulator-full barriers of both CTAs (one commit per barrier, by its
-//     cluster address).
+//   * The even CTA's MMA warp runs the schedule; its lane 0 issues the MMAs
+//     and commits each stage to the empty barriers of both CTAs and each
+//     finished accumulator to the accumulator-full barriers of both CTAs (one
+//     multicast commit reaching the barrier at the same offset in each CTA).
 //   * Each CTA's epilogue reads its 128 rows of the fp32 accumulator from its
 //     own tensor memory, narrows them once to fp16 and writes them with TMA
-//     stores through swizzled staging buffers; each epilogue warp arrives on
-//     the even CTA's accumulator-empty barrier as soon as its reads are done.
+//     stores of 32-row x 32-column blocks through swizzled staging buffers;
+//     each epilogue warp arrives on the even CTA's accumulator-empty barrier
+//     as soon as its reads are done.
 //   * Tensor memory (2 x 256 fp32 columns, double buffered) is allocated and
 //     freed by one warp of each CTA together (cta_group::2).
 // Tail: when the last partial wave of tiles would leave more than half of the
