@@ -13,7 +13,7 @@
 //     64 k-values for the same 128 x 256 x 64 of work that costs 48 KiB alone.
 //   * Both CTAs' TMA loads complete on the even CTA's full barrier, which the
 //     even CTA arms with the pair's total byte count.
-//   * The even CTA's MMA warp runs the schedule; its lane 0 issues the MMAs
+//   * The even CTA's MMA warp runs the schedule; one elected lane issues the MMAs
 //     and commits each stage to the empty barriers of both CTAs and each
 //     finished accumulator to the accumulator-full barriers of both CTAs (one
 //     multicast commit reaching the barrier at the same offset in each CTA).
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
-        // The whole warp runs the schedule; lane 0 issues.
+        // The whole warp runs the schedule; one lane, elected with elect.sync, issues.
         if (p.num_k_tiles > 0 && p.fault_mode != 1) {
             const uint32_t full0_even = map_shared_to_rank(smem_addr(&full[0]), 0);
             int stage = 0;
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     if (!ok) break;
                     const uint32_t fb = full0_even + 8u * static_cast<uint32_t>(stage);
                     const int32_t k0 = kt * Cfg::TK;
-                    if (lane == 0) {
+                    if (elect_one()) {
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
 #pragma unroll
                         for (int j = 0; j < Cfg::TK / 64; ++j)
@@ -215,8 +215,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
-        // The whole warp runs the schedule and computes the descriptors; lane 0
-        // issues the MMAs and the commits (tcgen05.commit tracks the MMAs of the
+        // The whole warp runs the schedule and computes the descriptors; one
+        // elected lane (elect.sync: the same lane every time in the converged
+        // warp) issues the MMAs and the commits, including the accumulator's
+        // commit after the last k step (tcgen05.commit tracks the MMAs of the
         // thread that issues it).
         if (rank == 0 && p.num_k_tiles > 0) {
             int stage = 0;
@@ -245,11 +247,13 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                                                 kSwizzle128B);
                         bd[kk] = make_smem_desc(b_s + kk * Cfg::B_KSTEP, Cfg::B_LBO, Cfg::B_SBO, kSwizzle128B);
                     }
-                    if (lane == 0) {
+                    if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < Cfg::TK / 16; ++kk)
                             tc_mma_f16_ss_pair(d_tmem, ad[kk], bd[kk], idesc, (kt > 0 || kk > 0) ? 1u : 0u);
                         tc_commit_pair_multicast(smem_addr(&empty[stage]), 0x3);  // the stage is free in both CTAs
+                        if (kt == p.num_k_tiles - 1)  // accumulator complete, in both CTAs
+                            tc_commit_pair_multicast(smem_addr(&acc_full[buf]), 0x3);
                     }
                     __syncwarp();
                     if (++stage == Cfg::STAGES) {
@@ -258,8 +262,6 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                if (lane == 0) tc_commit_pair_multicast(smem_addr(&acc_full[buf]), 0x3);  // accumulator complete
-                __syncwarp();
                 if (++buf == 2) {
                     buf = 0;
                     acc_phase ^= 1u;
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 }
             }
             // every MMA issued above has finished before tensor memory is freed
-            if (lane == 0) {
+            if (elect_one()) {
                 tc_commit_pair(map_shared_to_rank(smem_addr(drain), 0));
                 wait_phase_drain(drain, 0u, w);
             }

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 ok = warp_wait_phase(&empty[stage], phase ^ 1u, w, kWhereProducer);
                 if (!ok) break;
                 const int32_t k0 = kt * Cfg::TK;
-                if (lane == 0) {
+                if (elect_one()) {
                     mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_TX);
                     tma_load_2d(sA + stage * Cfg::A_STAGE, &tmap_a, &full[stage], k0, m0);
 #pragma unroll
@@ -177,11 +177,12 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     ad[kk] = make_smem_desc(a_s + kk * Cfg::A_KSTEP, 16u, Cfg::A_SBO, Cfg::A_SWIZZLE);
                     bd[kk] = make_smem_desc(b_s + kk * Cfg::B_KSTEP, Cfg::B_LBO, Cfg::B_SBO, kSwizzle128B);
                 }
-                if (lane == 0) {
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < Cfg::TK / 16; ++kk)
                         tc_mma_f16_ss(tmem_base, ad[kk], bd[kk], Cfg::IDESC, (kt > kt0 || kk > 0) ? 1u : 0u);
                     tc_commit(&empty[stage]);
+                    if (kt == kt1 - 1) tc_commit(&acc_full[0]);  // the partial accumulator is complete
                 }
                 __syncwarp();
                 if (++stage == Cfg::STAGES) {
@@ -189,8 +190,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     phase ^= 1u;
                 }
             }
-            if (ok && lane == 0) tc_commit(&acc_full[0]);  // the partial accumulator is complete
-            if (lane == 0) {
+            if (elect_one()) {
                 tc_commit(drain);
                 wait_phase_drain(drain, 0u, w);
             }
