@@ -312,10 +312,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const uint32_t t_row =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf) * Cfg::ACC_COLS;
             const uint32_t release_addr = acc_empty0_even + 8u * static_cast<uint32_t>(buf);
+            // The accumulator's tensor-memory reads are complete (tcgen05.wait::ld)
+            // before the arrive: a relaxed arrive orders nothing else that the MMA
+            // warp depends on, and a release at cluster scope measured 3-14 %
+            // slower where the epilogue is exposed (few k steps per tile).
             const auto release = [&]() {
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(release_addr);
+                if (lane == 0) mbar_arrive_cluster_relaxed(release_addr);
             };
             const int32_t c_row0 = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + q * 32;
             if (un.half < 0)
