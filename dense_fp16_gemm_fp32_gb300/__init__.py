@@ -41,6 +41,7 @@ from ._binding import (  # noqa: F401
     softmax_launch_count,
     softmax_plan,
     status_string,
+    tile_map_host,
     tile_schedule,
     tile_shape,
     workspace_bytes,

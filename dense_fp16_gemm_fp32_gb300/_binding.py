@@ -58,6 +58,8 @@ _SIGNATURES = {
                                        _c_void_p, _c_void_p, _c_void_p]),
     "gemm_tile_schedule": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_int32, _c_void_p, _c_void_p, _c_void_p]),
+    "gemm_tile_map_host": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _c_void_p, _c_void_p]),
     "gemm_query_status": (ctypes.c_int, [_c_void_p]),
     "gemm_launch_plan": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                         _c_void_p, _c_void_p, _c_void_p]),
@@ -274,6 +276,20 @@ def tile_schedule(M: int, N: int, tile_m: int, tile_n: int, group_size_m: int, d
                                        _stream_ptr(device))
     _check(rc, "gemm_tile_schedule")
     return pm[:n], pn[:n]
+
+
+def tile_map_host(M: int, N: int, tile_m: int, tile_n: int, group_size_m: int, pid0: int = 0, count=None):
+    """(pid_m, pid_n) int32 numpy arrays of the kernels' grouped map evaluated on the host
+    for pids [pid0, pid0 + count) (default: every tile). Needs no GPU."""
+    import numpy as np
+
+    n = -(-M // tile_m) * -(-N // tile_n) if M > 0 and N > 0 else 0
+    count = n - pid0 if count is None else count
+    pm = np.zeros(max(count, 1), dtype=np.int32)
+    pn = np.zeros(max(count, 1), dtype=np.int32)
+    rc = load().gemm_tile_map_host(M, N, tile_m, tile_n, group_size_m, pid0, count, pm.ctypes.data, pn.ctypes.data)
+    _check(rc, "gemm_tile_map_host")
+    return pm[:count], pn[:count]
 
 
 def query_status(device=None) -> int:

@@ -306,6 +306,7 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     p.num_tiles = static_cast<int32_t>(num_tiles);
     p.num_k_tiles = static_cast<int32_t>((pr.K + Cfg::TK - 1) / Cfg::TK);
     p.group_size_m = pr.group_size_m > p.num_pid_m ? p.num_pid_m : pr.group_size_m;
+    p.map = make_tile_map(p.num_pid_m, p.num_pid_n, p.group_size_m);
     p.status = d->status;
     p.trace = trace;
     p.watchdog_ns = watchdog_ns();
@@ -417,6 +418,7 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     p.num_tiles = static_cast<int32_t>(num_tiles);
     p.num_k_tiles = static_cast<int32_t>((pr.K + Cfg::TK - 1) / Cfg::TK);
     p.group_size_m = pr.group_size_m > p.num_pid_m ? p.num_pid_m : pr.group_size_m;
+    p.map = make_tile_map(p.num_pid_m, p.num_pid_n, p.group_size_m);
     p.status = d->status;
     p.trace = trace;
     p.watchdog_ns = watchdog_ns();
@@ -496,6 +498,7 @@ int launch_splitk(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t st
     p.num_tiles = static_cast<int32_t>(num_tiles);
     p.num_k_tiles = static_cast<int32_t>(k_tiles);
     p.group_size_m = pr.group_size_m > p.num_pid_m ? p.num_pid_m : pr.group_size_m;
+    p.map = make_tile_map(p.num_pid_m, p.num_pid_n, p.group_size_m);
     p.status = d->status;
     p.trace = trace;
     p.watchdog_ns = watchdog_ns();
@@ -866,11 +869,31 @@ int gemm_tile_schedule(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n, int
     const int64_t blocks64 = (num_tiles + threads - 1) / threads;
     const unsigned blocks = static_cast<unsigned>(blocks64 < 65535 ? blocks64 : 65535);
     tile_schedule_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<int32_t>(num_tiles), static_cast<int32_t>(num_pid_m), static_cast<int32_t>(num_pid_n), g, d_pid_m,
-        d_pid_n);
+        static_cast<int32_t>(num_tiles), make_tile_map(static_cast<int32_t>(num_pid_m), static_cast<int32_t>(num_pid_n), g),
+        d_pid_m, d_pid_n);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
+    return GEMM_OK;
+}
+
+int gemm_tile_map_host(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n, int32_t group_size_m, int64_t pid0,
+                       int32_t count, int32_t* pid_m, int32_t* pid_n)
+{
+    if (M < 0 || N < 0 || tile_m <= 0 || tile_n <= 0 || group_size_m <= 0 || count < 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t num_pid_m = (M + tile_m - 1) / tile_m;
+    const int64_t num_pid_n = (N + tile_n - 1) / tile_n;
+    const int64_t num_tiles = num_pid_m * num_pid_n;
+    if (num_tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    if (count == 0) return GEMM_OK;
+    if (pid_m == nullptr || pid_n == nullptr || pid0 < 0 || pid0 + count > num_tiles) return GEMM_ERR_INVALID_ARG;
+    const int32_t g = group_size_m > num_pid_m ? static_cast<int32_t>(num_pid_m) : group_size_m;
+    const TileMap map = make_tile_map(static_cast<int32_t>(num_pid_m), static_cast<int32_t>(num_pid_n), g);
+    for (int32_t i = 0; i < count; ++i) {
+        const TileCoord t = grouped_tile(static_cast<int32_t>(pid0 + i), map);
+        pid_m[i] = t.pid_m;
+        pid_n[i] = t.pid_n;
+    }
     return GEMM_OK;
 }
 
@@ -963,6 +986,7 @@ int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, in
     p.num_tiles = static_cast<int32_t>(num_tiles);
     p.num_k_tiles = static_cast<int32_t>((K + Cfg::TK - 1) / Cfg::TK);
     p.group_size_m = group_size_m > p.num_pid_m ? p.num_pid_m : group_size_m;
+    p.map = make_tile_map(p.num_pid_m, p.num_pid_n, p.group_size_m);
     p.status = d->scratch;  // word 0 of the static scratch array
     p.trace = nullptr;
     p.watchdog_ns = watchdog_ns();

@@ -113,16 +113,17 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31);
 
-    // Warp 0 works out its first tile (the grouped map's divisions take a few
-    // hundred cycles) while warp 2 initialises the barriers and warp 1
-    // allocates tensor memory.
+    // Prologue, shortest path to the first TMA load: thread 64 initialises the
+    // barriers while warp 0 maps its first tile; after one __syncthreads the
+    // producer starts, and warp 1 allocates tensor memory meanwhile, then
+    // meets the epilogue warps on named barrier 1 for its address.
     if (threadIdx.x == 0 && p.num_k_tiles > 0 && !Cfg::kGeneric) {
         tma_prefetch_desc(&tmap_a);
         tma_prefetch_desc(&tmap_b);
         tma_prefetch_desc(&tmap_c);
     }
     TileCoord first_tc{0, 0};
-    if (warp == 0) first_tc = grouped_tile(static_cast<int32_t>(blockIdx.x), p.num_pid_m, p.num_pid_n, p.group_size_m);
+    if (warp == 0) first_tc = grouped_tile(static_cast<int32_t>(blockIdx.x), p.map);
     if (threadIdx.x == 64) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(&full[s], Cfg::FULL_ARRIVALS);
@@ -136,14 +137,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-        tmem_relinquish_alloc_permit();
-    }
-    tc_fence_before_sync();
     __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    uint32_t tmem_base = 0;
+    if (warp >= 1 && warp < 2 + Cfg::EPI_WARPS) {  // warp 1 and the epilogue warps
+        if (warp == 1) {
+            tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+            tmem_relinquish_alloc_permit();
+        }
+        tc_fence_before_sync();
+        named_barrier_sync(1, 32 * (1 + Cfg::EPI_WARPS));
+        tc_fence_after_sync();
+        tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    }
     const Watch w{abort_flag, p.status, p.watchdog_ns};
 
     if (Cfg::kGeneric && (warp == 0 || warp >= 6)) {
@@ -158,7 +163,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const uint32_t a_base = smem_addr(sA);
             const uint32_t b_base = smem_addr(sB);
             for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
+                const TileCoord tc = grouped_tile(tile, p.map);
                 for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
                     ok = warp_wait_phase(&empty[stage], phase ^ 1u, w, kWhereProducer);
                     if (!ok) break;
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 const TileCoord tc = tile == static_cast<int32_t>(blockIdx.x)
                                          ? first_tc
-                                         : grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
+                                         : grouped_tile(tile, p.map);
                 const int32_t m0 = tc.pid_m * Cfg::TM;
                 const int32_t n0 = tc.pid_n * Cfg::TN;
                 for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         int buf = 0;
         uint32_t acc_phase = 0;
         for (int32_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-            const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
+            const TileCoord tc = grouped_tile(tile, p.map);
             if (p.trace != nullptr && warp == 2 && lane == 0) {
                 p.trace[3 * static_cast<int64_t>(tile) + 0] = tc.pid_m;
                 p.trace[3 * static_cast<int64_t>(tile) + 1] = tc.pid_n;
@@ -361,12 +366,11 @@ __global__ void __launch_bounds__(256) copy_rows_f16_kernel(const uint16_t* __re
 }
 
 // The grouped map alone, one thread per pid (same device function as above).
-__global__ void tile_schedule_kernel(int32_t num_tiles, int32_t num_pid_m, int32_t num_pid_n, int32_t group_size_m,
-                                     int32_t* pid_m, int32_t* pid_n)
+__global__ void tile_schedule_kernel(int32_t num_tiles, const TileMap map, int32_t* pid_m, int32_t* pid_n)
 {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t pid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; pid < num_tiles; pid += stride) {
-        const TileCoord t = grouped_tile(static_cast<int32_t>(pid), num_pid_m, num_pid_n, group_size_m);
+        const TileCoord t = grouped_tile(static_cast<int32_t>(pid), map);
         pid_m[pid] = t.pid_m;
         pid_n[pid] = t.pid_n;
     }

@@ -102,7 +102,7 @@ __device__ __forceinline__ PairUnit pair_unit(int32_t u, const GemmParams& p)
         r.pid = p.num_full_tiles + (v >> 1);
         r.half = v & 1;
     }
-    r.tc = grouped_tile(r.pid, p.num_pid_m, p.num_pid_n, p.group_size_m);
+    r.tc = grouped_tile(r.pid, p.map);
     return r;
 }
 
@@ -132,16 +132,18 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     const int32_t pair = static_cast<int32_t>(blockIdx.x >> 1);
     const int32_t num_pairs = static_cast<int32_t>(gridDim.x >> 1);
 
-    // Warp 0 works out its first unit (the grouped map's divisions take a few
-    // hundred cycles) while warp 2 initialises the barriers and warp 1
-    // allocates tensor memory.
+    // Prologue, shortest path to the first TMA load: thread 64 initialises the
+    // barriers and every thread arrives on the cluster barrier at once; warp
+    // 0 maps its first unit and warp 1 allocates the pair's tensor memory
+    // before waiting on it. The cluster barrier (both CTAs' barriers exist
+    // before either CTA signals the other) is all the producer waits for; the
+    // MMA and epilogue warps then meet warp 1 on named barrier 1 for the
+    // tensor-memory address.
     if (threadIdx.x == 0 && p.num_k_tiles > 0) {
         tma_prefetch_desc(&tmap_a);
         tma_prefetch_desc(&tmap_b);
         tma_prefetch_desc(&tmap_c);
     }
-    PairUnit first_un{};
-    if (warp == 0) first_un = pair_unit(pair, p);
     if (threadIdx.x == 64) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(&full[s], 1);   // even CTA: one arrive (with the pair's byte count)
@@ -155,16 +157,21 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         *abort_flag = 0u;
         fence_mbar_init();
     }
+    cluster_arrive();
+    PairUnit first_un{};
+    if (warp == 0) first_un = pair_unit(pair, p);
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
         tmem_relinquish_alloc_permit_pair();
     }
-    tc_fence_before_sync();
-    __syncthreads();
-    cluster_arrive();  // both CTAs' barriers exist before either signals the other
     cluster_wait();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    uint32_t tmem_base = 0;
+    if (warp >= 1) {  // warp 1 and the epilogue warps
+        tc_fence_before_sync();
+        named_barrier_sync(1, 32 * (1 + Cfg::EPI_WARPS));
+        tc_fence_after_sync();
+        tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    }
     const Watch w{abort_flag, p.status, p.watchdog_ns};
 
     if (warp == 0) {

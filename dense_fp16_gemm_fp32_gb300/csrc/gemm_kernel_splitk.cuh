@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     static_assert(S == 2 || S == 4 || S == 8, "cluster of 2, 4 or 8 CTAs");
     const int32_t rank = static_cast<int32_t>(cluster_ctarank());
     const int32_t tile = static_cast<int32_t>(blockIdx.x) / S;
-    const TileCoord tc = grouped_tile(tile, p.num_pid_m, p.num_pid_n, p.group_size_m);
+    const TileCoord tc = grouped_tile(tile, p.map);
     const int32_t m0 = tc.pid_m * Cfg::TM;
     const int32_t n0 = tc.pid_n * Cfg::TN;
     const int32_t per = (p.num_k_tiles + S - 1) / S;

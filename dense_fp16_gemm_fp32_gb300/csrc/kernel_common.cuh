@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "ptx.cuh"
+#include "tile_map.cuh"
 
 #include <cuda.h>
 
@@ -21,6 +22,7 @@ struct GemmParams {
     int32_t M, N, K;
     int32_t num_pid_m, num_pid_n, num_tiles, num_k_tiles;
     int32_t group_size_m;  // already clamped to [1, num_pid_m]
+    TileMap map;           // the grouped map's divisors for this launch
     uint32_t* status;
     int32_t* trace;  // NULL or 3 * num_tiles entries
     uint64_t watchdog_ns;

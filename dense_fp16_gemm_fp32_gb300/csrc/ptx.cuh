@@ -202,6 +202,13 @@ __device__ __forceinline__ bool elect_one()
     return pred != 0;
 }
 
+// Named barrier `id` (1..15; 0 is __syncthreads) over `threads` threads, a
+// multiple of 32: every warp that takes part executes it.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ---------------------------------------------------------------- clusters and CTA pairs
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {

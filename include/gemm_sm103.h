@@ -245,6 +245,21 @@ int gemm_tile_schedule(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n, int
                        int32_t* d_pid_m, int32_t* d_pid_n, void* stream);
 
 /*
+ * The same grouped map evaluated on the host by the same function the
+ * kernels use (the group and band divisions as multiply-shift divisions by
+ * constants fixed for the launch), for pids [pid0, pid0 + count): writes
+ * pid_m[i], pid_n[i] for pid pid0 + i to HOST arrays of `count` entries.
+ * Needs no GPU; for checking the map against an independent implementation.
+ * Source: as gemm_tile_schedule.
+ *   M, N, tile_m, tile_n, group_size_m   as for gemm_tile_schedule
+ * Returns GEMM_ERR_INVALID_ARG for bad extents, a negative count, NULL
+ * outputs with count > 0, or a range outside [0, tiles);
+ * GEMM_ERR_UNSUPPORTED if the tile count exceeds INT32_MAX.
+ */
+int gemm_tile_map_host(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n, int32_t group_size_m, int64_t pid0,
+                       int32_t count, int32_t* pid_m, int32_t* pid_n);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. Returns GEMM_ERR_TIMEOUT if a kernel launched since the last query
  * gave up on a bounded wait (its output is then incomplete), GEMM_OK
