@@ -393,12 +393,15 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     const int64_t num_tiles = num_pid_m * num_pid_n;
     if (num_tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
 
-    CUtensorMap ma, mb, mc;
+    CUtensorMap ma, mb, mc, mc_last;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
-    // C: EPI_COLS x 32-row store boxes with the epilogue staging's swizzle
-    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, Cfg::EPI_COLS, 32,
-                  Cfg::EPI_COLS == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    // C: 32-row store boxes, EPI_COLS (EPI_COLS_LAST for each pair's last
+    // unit) wide, with the epilogue staging's swizzle
+    static_assert(Cfg::EPI_COLS == 32 && Cfg::EPI_COLS_LAST == 64, "box widths and swizzles below");
+    rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (rc != GEMM_OK) return rc;
+    rc = make_map(&mc_last, pr.C, pr.N, pr.M, pr.ldc, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != GEMM_OK) return rc;
     if (pr.K > 0) {
         rc = make_map(&ma, pr.A, pr.K, pr.M, pr.lda, 64, Cfg::CTA_M, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -437,7 +440,7 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     lc.stream = stream;
     lc.attrs = &attr;
     lc.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, ma, mb, mc, p);
+    const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, ma, mb, mc, mc_last, p);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
     return GEMM_OK;
