@@ -203,31 +203,49 @@ int32_t tuned_cfg(int64_t M, int64_t N, int64_t K)
     return it == g_tuned.end() ? GEMM_TILE_AUTO : it->second;
 }
 
-// Below this many 256 x 256 tiles, fewer than half of the 76 CTA pairs of a
-// GB300 would have work: the one-CTA 128 x 128 tile spreads the problem over
-// four times as many SMs (measured faster at 512^3, 1024x768x128, 1024^3).
+// The untuned rule of GEMM_TILE_AUTO, from device times per call of every
+// configuration on one GB300 (CUDA graphs; the workload shapes, square
+// 512..16384, and low-K variants of them):
+//  * few 128 x 128 tiles (at most kSplitKMaxTiles, a quarter of the SMs) with
+//    a long K (at least kSplitKMinK): split-K across a cluster
+//    (128x4096x4096: 10.1 us against 23.1 us for the one-CTA 128 x 256 tile);
+//  * at most one 128-row band: the one-CTA 128 x 256 tile (half of every
+//    pair tile would be empty);
+//  * fewer than kFewPairTiles 256 x 256 tiles (fewer than half of the 76 CTA
+//    pairs busy): the CTA-pair 128-deep tile when K >= 1024 (1024^3: 6.7 us
+//    against 7.7), else the one-CTA 128 x 128 tile, four times as many tiles
+//    (512^3, 1024x768x128);
+//  * less than one wave of pair tiles (kOnePairWave), or K <= kShortK: the
+//    one-CTA 128 x 256 tile, whose epilogue and operand loads suit few k steps
+//    (2048^3 14.6 us, 4096x3072x128 8.0 us against 9.2 for the pair tile);
+//  * otherwise the CTA-pair tile: 64-deep stages (six) up to K = kDeepK
+//    (4096^3 75.7 us against 77.2, ragged 4095x3000x1000 25.9 against 26.2),
+//    128-deep stages (three) above it (16384^3 5141 us against 5359; equal
+//    per unit of power at 8192^3, where both run power-capped).
+constexpr int64_t kSplitKMaxTiles = 38;
+constexpr int64_t kSplitKMinK = 2048;
 constexpr int64_t kFewPairTiles = 32;
-// Below this many (less than one wave of the 76 resident CTA pairs), the
-// one-CTA 128 x 256 tile, twice as many tiles over the 152 SMs, finishes first
-// (measured at 2048^3: 14.1 us against 15.7 us for the pair tile).
 constexpr int64_t kOnePairWave = 76;
+constexpr int64_t kShortK = 256;
+constexpr int64_t kDeepK = 4096;
+
+int auto_cfg(int64_t M, int64_t N, int64_t K)
+{
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    const int64_t small_tiles = ((M + 127) / 128) * ((N + 127) / 128);
+    if (small_tiles <= kSplitKMaxTiles && K >= kSplitKMinK) return GEMM_TILE_128x128x64_SPLITK;
+    if (M <= 128) return GEMM_TILE_128x256x64;
+    if (pair_tiles < kFewPairTiles) return K >= 1024 ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x128x64;
+    if (pair_tiles < kOnePairWave || K <= kShortK) return GEMM_TILE_128x256x64;
+    return K <= kDeepK ? GEMM_TILE_256x256x64_PAIR : GEMM_TILE_256x256x128_PAIR;
+}
 
 // GEMM_TILE_AUTO: the configuration gemm_autotune chose for this shape on
-// the current device, if any; else the one-CTA 128 x 256 tile when the
-// problem has at most one 128-row band (half of every pair tile would be
-// empty), the one-CTA 128 x 128 tile when it has fewer than kFewPairTiles
-// 256 x 256 tiles, the one-CTA 128 x 256 tile when it has less than one wave
-// of them, and the CTA-pair 256 x 256 tile with 128-deep k steps otherwise.
+// the current device, if any; else auto_cfg.
 int resolve_cfg(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tm, int32_t* tn, int32_t* tk)
 {
     if (tile_cfg == GEMM_TILE_AUTO) tile_cfg = tuned_cfg(M, N, K);
-    if (tile_cfg == GEMM_TILE_AUTO) {
-        const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-        tile_cfg = M <= 128                     ? GEMM_TILE_128x256x64
-                   : pair_tiles < kFewPairTiles ? GEMM_TILE_128x128x64
-                   : pair_tiles < kOnePairWave  ? GEMM_TILE_128x256x64
-                                                : GEMM_TILE_256x256x128_PAIR;
-    }
+    if (tile_cfg == GEMM_TILE_AUTO) tile_cfg = auto_cfg(M, N, K);
     switch (tile_cfg) {
         case GEMM_TILE_128x256x64:
             *tm = Cfg128x256::TM, *tn = Cfg128x256::TN, *tk = Cfg128x256::TK;

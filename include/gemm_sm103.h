@@ -66,10 +66,13 @@ typedef enum {
 /* Tile configurations (TILE_M x TILE_N x TILE_K). */
 typedef enum {
     GEMM_TILE_AUTO = 0,       /* the library picks: the configuration gemm_autotune chose for
-                                 this (M, N, K) on the current device; else 128x256x64 when
-                                 M <= 128, 128x128x64 when the problem has fewer than 32
-                                 tiles of 256x256, 128x256x64 when it has fewer than 76 (less
-                                 than one wave of CTA pairs), and 256x256x128_PAIR otherwise */
+                                 this (M, N, K) on the current device; else 128x128x64_SPLITK
+                                 when there are at most 38 tiles of 128x128 and K >= 2048;
+                                 128x256x64 when M <= 128; with fewer than 32 tiles of
+                                 256x256, 256x256x128_PAIR if K >= 1024, else 128x128x64;
+                                 128x256x64 with fewer than 76 (less than one wave of CTA
+                                 pairs) or K <= 256; otherwise 256x256x64_PAIR up to
+                                 K = 4096 and 256x256x128_PAIR above */
     GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */
     GEMM_TILE_128x64x32 = 2,  /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
                                  BLOCK_SIZE_N 64, BLOCK_SIZE_K 32) */

@@ -41,10 +41,16 @@ def test_status_strings(lib):
 def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_AUTO, M=128) == (128, 256, 64)
     assert g.tile_shape(g.TILE_AUTO, M=129, N=8192) == (128, 256, 64)    # 32 pair tiles: under one wave
-    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2048) == (128, 256, 64)   # 64 pair tiles
-    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560) == (256, 256, 128)  # 80 pair tiles
-    assert g.tile_shape(g.TILE_AUTO, M=512, N=512) == (128, 128, 64)      # 4 pair tiles: few
+    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2048, K=2048) == (128, 256, 64)   # 64 pair tiles
+    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4096) == (256, 256, 64)   # 80 pair tiles, K <= 4096
+    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4097) == (256, 256, 128)  # deeper K
+    assert g.tile_shape(g.TILE_AUTO, M=4096, N=3072, K=256) == (128, 256, 64)    # few k steps
+    assert g.tile_shape(g.TILE_AUTO, M=512, N=512, K=512) == (128, 128, 64)      # 4 pair tiles: few
+    assert g.tile_shape(g.TILE_AUTO, M=1024, N=1024, K=1024) == (256, 256, 128)  # few, long enough K
+    assert g.tile_shape(g.TILE_AUTO, M=1024, N=768, K=128) == (128, 128, 64)
+    assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=4096) == (128, 128, 64)    # split-K
     assert g.tile_shape(g.TILE_AUTO, M=8192, N=8192, K=8192) == (256, 256, 128)
+    assert g.tile_shape(g.TILE_AUTO, M=16384, N=16384, K=16384) == (256, 256, 128)
     assert g.tile_shape(g.TILE_256x256x64_PAIR) == (256, 256, 64)
     assert g.tile_shape(g.TILE_256x256x128_PAIR) == (256, 256, 128)
     assert g.tile_shape(g.TILE_128x256x64) == (128, 256, 64)

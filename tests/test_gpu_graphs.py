@@ -30,7 +30,7 @@ def capture(fn):
 
 
 @pytest.mark.parametrize("M,N,K,cfg", [
-    (2048, 2048, 1024, g.TILE_AUTO),                   # the pair kernel
+    (4096, 2048, 1024, g.TILE_AUTO),                   # the pair kernel (64-deep stages)
     (300, 520, 264, g.TILE_128x128x64),
     (512, 512, 512, g.TILE_128x128x64_SPLITK),         # cluster split-K
     (1000, 37, 1000, g.TILE_AUTO),                     # N not a multiple of 8: the workspace route
