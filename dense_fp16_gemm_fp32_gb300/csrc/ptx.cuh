@@ -98,13 +98,6 @@ __device__ __forceinline__ void bulk_wait_group_read()
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
-// Wait until at most N of this thread's bulk groups are incomplete.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group()
-{
-    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -217,13 +210,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
-__device__ __forceinline__ uint32_t cluster_nctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_shared_to_rank(uint32_t saddr, uint32_t rank)
 {
@@ -259,12 +245,6 @@ __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr)
                  : "r"(cluster_addr)
                  : "memory");
     return v;
-}
-
-// Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Arrive on an mbarrier given by its shared::cluster address, with no memory
