@@ -272,6 +272,23 @@ int resolve_cfg(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tm, 
     }
 }
 
+#ifndef GEMM_PDL
+#define GEMM_PDL 1  // measured: 1024^3 6.67 -> 5.73 us, 4096^3 76.8 -> 75.2 us in back-to-back calls
+#endif
+
+// Programmatic dependent launch: the GEMM kernels call
+// griddepcontrol.launch_dependents on entry and griddepcontrol.wait before
+// their first access to global memory, so a GEMM launched with this
+// attribute may be scheduled while the previous kernel of the stream is
+// still running (on the SMs it leaves free) and run its prologue there.
+cudaLaunchAttribute pdl_attr()
+{
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    return attr;
+}
+
 template <class Cfg>
 int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
 {
@@ -340,8 +357,15 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
 
     const int64_t slots = static_cast<int64_t>(d->sm_count) * d->ctas_per_sm[cfg_id];
     const unsigned grid = static_cast<unsigned>(num_tiles < slots ? num_tiles : slots);
-    kernel<<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(ma, mb, mc, p);
-    const cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attrs[1] = {pdl_attr()};
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(grid, 1, 1);
+    lc.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = stream;
+    lc.attrs = attrs;
+    lc.numAttrs = GEMM_PDL ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, ma, mb, mc, p);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
     return GEMM_OK;
@@ -458,8 +482,9 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     lc.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
     lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
     lc.stream = stream;
-    lc.attrs = &attr;
-    lc.numAttrs = 1;
+    cudaLaunchAttribute attrs[2] = {attr, pdl_attr()};
+    lc.attrs = attrs;
+    lc.numAttrs = GEMM_PDL ? 2 : 1;
     const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, ma, mb, mc, mc_last, p);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
@@ -541,8 +566,9 @@ int launch_splitk(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t st
     lc.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
     lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
     lc.stream = stream;
-    lc.attrs = &attr;
-    lc.numAttrs = 1;
+    cudaLaunchAttribute attrs[2] = {attr, pdl_attr()};
+    lc.attrs = attrs;
+    lc.numAttrs = GEMM_PDL ? 2 : 1;
     const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, ma, mb, p);
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);

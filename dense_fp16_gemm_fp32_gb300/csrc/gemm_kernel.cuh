@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     gemm_f16_f32acc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                            const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
 {
+    griddep_launch_dependents();  // the next kernel in the stream may start its prologue
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // swizzled tiles need 1024 B alignment
@@ -149,6 +150,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         tc_fence_after_sync();
         tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     }
+    // launched with programmatic stream serialisation, this grid may start
+    // while the previous kernel in the stream runs: nothing below touches
+    // global memory before that kernel has completed
+    griddep_wait();
     const Watch w{abort_flag, p.status, p.watchdog_ns};
 
     if (Cfg::kGeneric && (warp == 0 || warp >= 6)) {

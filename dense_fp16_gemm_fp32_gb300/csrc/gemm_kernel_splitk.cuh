@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 {
     static_assert(Cfg::TM == 128 && Cfg::TK == 64 && !Cfg::kGeneric, "one-CTA TMA tile");
     static_assert(Cfg::STAGES * Cfg::A_STAGE >= Cfg::TM * Cfg::TN * 4, "the partial tile fits in the A ring");
+    griddep_launch_dependents();  // the next kernel in the stream may start its prologue
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -123,6 +124,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    // launched with programmatic stream serialisation, this grid may start
+    // while the previous kernel in the stream runs: nothing below touches
+    // global memory before that kernel has completed
+    griddep_wait();
     const Watch w{abort_flag, p.status, p.watchdog_ns};
 
     if (warp == 0) {
