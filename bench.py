@@ -364,7 +364,7 @@ def run_ours(args, w, rank, world, local_rank):
     return 0
 
 
-def pipelined_e2e(steps, dev, world, host_in, out_like, fn, label):
+def pipelined_e2e(steps, dev, world, host_in, out_like, fn, label, nbuf=2):
     """Steps of host inputs -> device -> fn -> host output, through the public
     API. Every step copies its own inputs in and its result out; copies of
     step i+1 and i-1 overlap the compute of step i (separate H2D, compute and
@@ -372,7 +372,6 @@ def pipelined_e2e(steps, dev, world, host_in, out_like, fn, label):
     import torch
 
     hin = [t.pin_memory() for t in host_in]
-    nbuf = 2
     din = [[torch.empty_like(t, device=dev) for t in hin] for _ in range(nbuf)]
     dout = [torch.empty_like(out_like, device=dev) for _ in range(nbuf)]
     hout = [torch.empty_like(out_like, device="cpu").pin_memory() for _ in range(nbuf)]
@@ -418,7 +417,7 @@ def pipelined_e2e(steps, dev, world, host_in, out_like, fn, label):
     s_out.wait_stream(s_comp)
     e1.record(s_out)
     torch.cuda.synchronize(dev)
-    return max_over_ranks(e0.elapsed_time(e1), dev, world), steps, f"pipelined: H2D, {label} and D2H streams, 2 buffers"
+    return max_over_ranks(e0.elapsed_time(e1), dev, world), steps, f"pipelined: H2D, {label} and D2H streams, {nbuf} buffers"
 
 
 def run_e2e(args, w, g, A, B, dev, world):
@@ -428,7 +427,7 @@ def run_e2e(args, w, g, A, B, dev, world):
     out_like = torch.empty((w.M, w.N), dtype=torch.float16)
     return pipelined_e2e(steps, dev, world, [A, B], out_like,
                          lambda ins, out: g.gemm(ins[0], ins[1], group_size_m=args.group_size_m, out=out,
-                                                 tile_cfg=args.tile_cfg), "GEMM")
+                                                 tile_cfg=args.tile_cfg), "GEMM", nbuf=args.e2e_buffers)
 
 
 # ---------------------------------------------------------------- softmax workloads
@@ -594,6 +593,8 @@ def main():
     p.add_argument("--tile-cfg", type=int, default=0)
     p.add_argument("--flush-l2", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--e2e-buffers", type=int, default=2,
+                   help="device and pinned host buffer sets the end-to-end leg rotates through")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--reference-budget-s", type=float, default=90.0)
