@@ -34,6 +34,16 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Work is
  *     enqueued asynchronously; no host synchronisation happens unless an entry
  *     point says so.
+ *   - The GEMM kernels are launched with programmatic stream serialisation
+ *     (programmatic dependent launch): a GEMM may be scheduled while the
+ *     previous kernel in its stream still runs, and reads its operands and
+ *     writes C only after that kernel has completed (griddepcontrol.wait), so
+ *     stream order holds as usual. They also allow the next kernel in the
+ *     stream to be scheduled early (griddepcontrol.launch_dependents on
+ *     entry); a following kernel that the caller launches with the same
+ *     attribute must wait the same way (griddepcontrol.wait or
+ *     cudaGridDependencySynchronize) before it reads C. Kernels launched
+ *     without that attribute are unaffected.
  *   - Return value: a gemm_status_t. Argument errors are detected on the host
  *     before anything is enqueued. GEMM_ERR_CUDA means a CUDA runtime call
  *     failed; gemm_last_cuda_error() returns its cudaError_t.
