@@ -28,7 +28,8 @@ TILE_256x256x64_PAIR = 3
 TILE_256x256x128_PAIR = 4
 TILE_128x128x64 = 5
 TILE_128x128x64_SPLITK = 6
-TILE_COUNT = 7
+TILE_128x64x64 = 7
+TILE_COUNT = 8
 
 DEFAULT_GROUP_SIZE_M = 8
 

@@ -24,8 +24,9 @@ using Cfg128x256 = TileCfg<128, 256, 64, 4>;
 using Cfg128x64 = TileCfg<128, 64, 32, 6>;
 using Cfg128x128 = TileCfg<128, 128, 64, 6>;
 using CfgSplitK = TileCfg<128, 128, 64, 4>;  // the ring also holds the 64 KiB fp32 partial tile
+using Cfg128x64x64 = TileCfg<128, 64, 64, 8>;
 using CfgGeneric = TileCfg<128, 256, 64, 4, true>;  // plain loads and stores (operands TMA cannot address)
-constexpr int kGenericCfgId = 7;
+constexpr int kGenericCfgId = 8;
 constexpr int kMaxSplitK = 8;  // portable cluster size
 using CfgPair256 = PairCfg<6>;
 using CfgPair256Deep = PairCfg<3, 128>;
@@ -35,7 +36,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumCfgs = 8;  // the tile configurations 1..6 and the generic-load kernel
+constexpr int kNumCfgs = 9;  // the tile configurations 1..7 and the generic-load kernel
 constexpr int64_t kMaxExtent = int64_t(1) << 30;
 constexpr uint64_t kDefaultWatchdogNs = 2000000000ull;
 
@@ -204,28 +205,37 @@ int32_t tuned_cfg(int64_t M, int64_t N, int64_t K)
 }
 
 // The untuned rule of GEMM_TILE_AUTO, from device times per call of every
-// configuration on one GB300 (CUDA graphs; the workload shapes, square
-// 512..16384, and low-K variants of them):
+// configuration on one GB300 (CUDA graphs, back-to-back calls overlapping
+// through programmatic dependent launch; the workload shapes, square
+// 512..16384, and low-K and few-tile variants of them). Problems with few
+// tiles are bound by each CTA's operand loads (about 60 bytes per cycle into
+// one SM), so there the tile that spreads the loads over the most SMs wins:
 //  * few 128 x 128 tiles (at most kSplitKMaxTiles, a quarter of the SMs) with
 //    a long K (at least kSplitKMinK): split-K across a cluster
 //    (128x4096x4096: 10.1 us against 23.1 us for the one-CTA 128 x 256 tile);
+//  * 128 x 64 tiles that fit one wave (kOneWave) with at most one 128-row band
+//    or K <= kSmallK: the one-CTA 128 x 64 x 64 tile (512^3 4.14 us against
+//    4.50 for the pair tile and 4.78 for 128 x 128; 1024x768x128 2.70 against
+//    3.10; 128x8192x256 3.26 against 4.57 for 128 x 256);
 //  * at most one 128-row band: the one-CTA 128 x 256 tile (half of every
 //    pair tile would be empty);
-//  * fewer than kFewPairTiles 256 x 256 tiles (fewer than half of the 76 CTA
-//    pairs busy): the CTA-pair 128-deep tile when K >= 1024 (1024^3: 6.7 us
-//    against 7.7), else the one-CTA 128 x 128 tile, four times as many tiles
-//    (512^3; 1024x768x128: 3.10 us against 3.29 for the notebook's 128 x 64 x 32
-//    tile, back-to-back calls overlapping through programmatic dependent launch);
-//  * less than one wave of pair tiles (kOnePairWave), or K <= kShortK: the
-//    one-CTA 128 x 256 tile, whose epilogue and operand loads suit few k steps
-//    (2048^3 14.6 us, 4096x3072x128 8.0 us against 9.2 for the pair tile);
+//  * at most kOnePairWave / 2 tiles of 256 x 256, each of which the pair
+//    kernel splits into two column halves (twice the SMs): the CTA-pair
+//    128-deep tile when K > kSmallK (2048x1024x1024 6.49 us against 8.34 for
+//    128 x 256; 768^3 4.96 against 5.22 for 128 x 64 x 64), else the one-CTA
+//    128 x 128 tile (2048x1024x512 4.96 against 5.05 for the pair tile);
+//  * less than one wave of pair tiles, or K <= kShortK: the one-CTA
+//    128 x 256 tile, whose epilogue and operand loads suit few k steps
+//    (4096x3072x128 7.25 us; with 40 to 64 pair tiles all of 128 x 256 and
+//    the two pair depths lie within 3 %);
 //  * otherwise the CTA-pair tile: 64-deep stages (six) up to K = kDeepK
 //    (4096^3 75.7 us against 77.2, ragged 4095x3000x1000 25.9 against 26.2),
 //    128-deep stages (three) above it (16384^3 5141 us against 5359; equal
 //    per unit of power at 8192^3, where both run power-capped).
 constexpr int64_t kSplitKMaxTiles = 38;
 constexpr int64_t kSplitKMinK = 2048;
-constexpr int64_t kFewPairTiles = 32;
+constexpr int64_t kOneWave = 152;
+constexpr int64_t kSmallK = 512;
 constexpr int64_t kOnePairWave = 76;
 constexpr int64_t kShortK = 256;
 constexpr int64_t kDeepK = 4096;
@@ -234,9 +244,11 @@ int auto_cfg(int64_t M, int64_t N, int64_t K)
 {
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     const int64_t small_tiles = ((M + 127) / 128) * ((N + 127) / 128);
+    const int64_t narrow_tiles = ((M + 127) / 128) * ((N + 63) / 64);
     if (small_tiles <= kSplitKMaxTiles && K >= kSplitKMinK) return GEMM_TILE_128x128x64_SPLITK;
+    if (narrow_tiles <= kOneWave && (M <= 128 || K <= kSmallK)) return GEMM_TILE_128x64x64;
     if (M <= 128) return GEMM_TILE_128x256x64;
-    if (pair_tiles < kFewPairTiles) return K >= 1024 ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x128x64;
+    if (2 * pair_tiles <= kOnePairWave) return K > kSmallK ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x128x64;
     if (pair_tiles < kOnePairWave || K <= kShortK) return GEMM_TILE_128x256x64;
     return K <= kDeepK ? GEMM_TILE_256x256x64_PAIR : GEMM_TILE_256x256x128_PAIR;
 }
@@ -266,6 +278,9 @@ int resolve_cfg(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tm, 
         case GEMM_TILE_128x128x64_SPLITK:
             *tm = CfgSplitK::TM, *tn = CfgSplitK::TN, *tk = CfgSplitK::TK;
             return GEMM_TILE_128x128x64_SPLITK;
+        case GEMM_TILE_128x64x64:
+            *tm = Cfg128x64x64::TM, *tn = Cfg128x64x64::TN, *tk = Cfg128x64x64::TK;
+            return GEMM_TILE_128x64x64;
         default:
             return -1;
     }
@@ -434,7 +449,7 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     const int64_t num_pid_m = (pr.M + Cfg::TM - 1) / Cfg::TM;
     const int64_t num_pid_n = (pr.N + Cfg::TN - 1) / Cfg::TN;
     const int64_t num_tiles = num_pid_m * num_pid_n;
-    if (num_tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    if (num_tiles + slots > INT32_MAX) return GEMM_ERR_UNSUPPORTED;  // units: tiles + split halves, < tiles + slots
 
     CUtensorMap ma, mb, mc, mc_last;
     std::memset(&ma, 0, sizeof(ma));
@@ -699,6 +714,8 @@ int dispatch_tma(const Problem& pr, int cfg, int32_t* trace, cudaStream_t s)
             return launch<Cfg128x128>(pr, cfg, trace, s);
         case GEMM_TILE_128x128x64_SPLITK:
             return launch_splitk(pr, cfg, trace, s);
+        case GEMM_TILE_128x64x64:
+            return launch<Cfg128x64x64>(pr, cfg, trace, s);
         default:
             return launch<Cfg128x256>(pr, cfg, trace, s);
     }
@@ -892,8 +909,11 @@ int gemm_launch_plan(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t*
                splitk_factor(tiles, (K + tk - 1) / tk, d->sm_count) > 1) {
         ctas = tiles * splitk_factor(tiles, (K + tk - 1) / tk, d->sm_count);  // one cluster per tile
     } else {
-        // one-CTA kernels: occupancy is set up on first launch; report the SM bound
-        const int64_t slots = static_cast<int64_t>(d->sm_count) * (d->attr_set[cfg] ? d->ctas_per_sm[cfg] : 1);
+        // one-CTA kernels (an unsplit split-K problem runs the 128 x 128 one);
+        // occupancy is set up on first launch: until then report the SM bound
+        const int occ_id = cfg == GEMM_TILE_128x128x64_SPLITK ? GEMM_TILE_128x128x64 : cfg;
+        const int per_sm = d->attr_set[occ_id] && d->ctas_per_sm[occ_id] > 0 ? d->ctas_per_sm[occ_id] : 1;
+        const int64_t slots = static_cast<int64_t>(d->sm_count) * per_sm;
         ctas = tiles < slots ? tiles : slots;
     }
     if (grid_ctas) *grid_ctas = static_cast<int32_t>(ctas);

@@ -196,10 +196,23 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
                     }
                 }
             }
+            if (!kDirect && lane == 0) bulk_commit_group();  // one group per block, as below
             continue;
         }
         const uint32_t buf = stage0 + static_cast<uint32_t>((c & 1) * St::BUF_BYTES);
-        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this buffer has read it
+        // The store that last used this buffer must have read it. Every block
+        // commits one bulk group (empty for blocks stored directly or outside
+        // C), so with an even number of blocks per tile the group that last
+        // used this buffer is the one before the latest (block c-1, or the
+        // previous tile's last block, used the other buffer); with an odd
+        // number, block 0 follows the previous tile's last block in the same
+        // buffer, so it waits for every group.
+        if (lane == 0) {
+            if ((TN / COLS) % 2 == 1 && c == 0)
+                bulk_wait_group_read<0>();
+            else
+                bulk_wait_group_read<1>();
+        }
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < St::CHUNKS; ++j)

@@ -78,11 +78,13 @@ typedef enum {
     GEMM_TILE_AUTO = 0,       /* the library picks: the configuration gemm_autotune chose for
                                  this (M, N, K) on the current device; else 128x128x64_SPLITK
                                  when there are at most 38 tiles of 128x128 and K >= 2048;
-                                 128x256x64 when M <= 128; with fewer than 32 tiles of
-                                 256x256, 256x256x128_PAIR if K >= 1024, else 128x128x64;
-                                 128x256x64 with fewer than 76 (less than one wave of CTA
-                                 pairs) or K <= 256; otherwise 256x256x64_PAIR up to
-                                 K = 4096 and 256x256x128_PAIR above */
+                                 128x64x64 when its tiles fit one wave (at most 152) and
+                                 M <= 128 or K <= 512; 128x256x64 when M <= 128; with at most
+                                 38 tiles of 256x256 (every one split into column halves),
+                                 256x256x128_PAIR if K > 512, else 128x128x64; 128x256x64
+                                 with fewer than 76 (less than one wave of CTA pairs) or
+                                 K <= 256; otherwise 256x256x64_PAIR up to K = 4096 and
+                                 256x256x128_PAIR above */
     GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */
     GEMM_TILE_128x64x32 = 2,  /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
                                  BLOCK_SIZE_N 64, BLOCK_SIZE_K 32) */
@@ -96,7 +98,10 @@ typedef enum {
                                  through distributed shared memory (S: the largest power of
                                  two <= 8 with S <= ceil(K/64) and tiles * S <= SMs; S = 1
                                  runs the 128x128x64 kernel) */
-    GEMM_TILE_COUNT = 7       /* number of values above, GEMM_TILE_AUTO included */
+    GEMM_TILE_128x64x64 = 7,  /* 1 CTA per tile, 8 stages of 64-deep k steps: four times the
+                                 tiles of 128x256 and A rows of 128 bytes, for problems whose
+                                 time is each CTA's operand loads */
+    GEMM_TILE_COUNT = 8       /* number of values above, GEMM_TILE_AUTO included */
 } gemm_tile_cfg_t;
 
 /*

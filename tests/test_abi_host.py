@@ -39,15 +39,20 @@ def test_status_strings(lib):
 
 
 def test_tile_shapes(lib):
-    assert g.tile_shape(g.TILE_AUTO, M=128) == (128, 256, 64)
-    assert g.tile_shape(g.TILE_AUTO, M=129, N=8192) == (128, 256, 64)    # 32 pair tiles: under one wave
+    assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=1024) == (128, 64, 64)     # one band, 64 tiles of 128x64
+    assert g.tile_shape(g.TILE_AUTO, M=128, N=16384, K=1024) == (128, 256, 64)   # one band, 256 tiles of 128x64
+    assert g.tile_shape(g.TILE_AUTO, M=129, N=8192, K=1024) == (256, 256, 128)   # 32 pair tiles: all split
+    assert g.tile_shape(g.TILE_AUTO, M=129, N=10240, K=1024) == (128, 256, 64)   # 40 pair tiles: under one wave
+    assert g.tile_shape(g.TILE_AUTO, M=2048, N=1024, K=512) == (128, 128, 64)    # 32 pair tiles, short K
     assert g.tile_shape(g.TILE_AUTO, M=2048, N=2048, K=2048) == (128, 256, 64)   # 64 pair tiles
     assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4096) == (256, 256, 64)   # 80 pair tiles, K <= 4096
     assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4097) == (256, 256, 128)  # deeper K
     assert g.tile_shape(g.TILE_AUTO, M=4096, N=3072, K=256) == (128, 256, 64)    # few k steps
-    assert g.tile_shape(g.TILE_AUTO, M=512, N=512, K=512) == (128, 128, 64)      # 4 pair tiles: few
+    assert g.tile_shape(g.TILE_AUTO, M=512, N=512, K=512) == (128, 64, 64)       # 32 tiles of 128x64, short K
+    assert g.tile_shape(g.TILE_AUTO, M=1024, N=1024, K=512) == (128, 64, 64)     # 128 of them: one wave
     assert g.tile_shape(g.TILE_AUTO, M=1024, N=1024, K=1024) == (256, 256, 128)  # few, long enough K
-    assert g.tile_shape(g.TILE_AUTO, M=1024, N=768, K=128) == (128, 128, 64)
+    assert g.tile_shape(g.TILE_AUTO, M=1024, N=768, K=128) == (128, 64, 64)
+    assert g.tile_shape(g.TILE_AUTO, M=1024, N=2048, K=256) == (128, 128, 64)    # 256 tiles of 128x64: two waves
     assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=4096) == (128, 128, 64)    # split-K
     assert g.tile_shape(g.TILE_AUTO, M=8192, N=8192, K=8192) == (256, 256, 128)
     assert g.tile_shape(g.TILE_AUTO, M=16384, N=16384, K=16384) == (256, 256, 128)
@@ -57,6 +62,7 @@ def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_128x64x32) == (128, 64, 32)
     assert g.tile_shape(g.TILE_128x128x64) == (128, 128, 64)
     assert g.tile_shape(g.TILE_128x128x64_SPLITK) == (128, 128, 64)
+    assert g.tile_shape(g.TILE_128x64x64) == (128, 64, 64)
     with pytest.raises(g.GemmError) as e:
         g.tile_shape(17)
     assert e.value.code == g.GEMM_ERR_UNSUPPORTED

@@ -4,8 +4,8 @@ write) and a later call overwrites an earlier call's input (write after
 read). The GEMM kernels are launched with programmatic stream serialisation,
 so a call may start while the previous one still runs; their results must be
 bit-identical to the same chain run with a synchronisation after every call.
-The shapes make consecutive calls run different kernels (one-CTA, CTA-pair,
-split-K)."""
+The shapes make consecutive calls run different kernels (one-CTA tiles of
+three widths, CTA-pair, split-K)."""
 import pytest
 import torch
 
@@ -19,7 +19,8 @@ LINKS = [
     (512, 2048, g.TILE_AUTO),                  # 1024 x 2048 x 512: one-CTA tiles (few k steps)
     (2048, 1024, g.TILE_256x256x64_PAIR),      # the CTA-pair kernel
     (1024, 128, g.TILE_128x128x64_SPLITK),     # few tiles: split-K across a cluster
-    (128, 1024, g.TILE_128x256x64),
+    (128, 512, g.TILE_128x256x64),
+    (512, 256, g.TILE_AUTO),                   # 1024 x 256 x 512: 32 tiles of 128 x 64
 ]
 M = 1024
 

@@ -33,6 +33,7 @@ def capture(fn):
     (4096, 2048, 1024, g.TILE_AUTO),                   # the pair kernel (64-deep stages)
     (300, 520, 264, g.TILE_128x128x64),
     (512, 512, 512, g.TILE_128x128x64_SPLITK),         # cluster split-K
+    (1024, 768, 128, g.TILE_AUTO),                     # 128 x 64 x 64 tiles
     (1000, 37, 1000, g.TILE_AUTO),                     # N not a multiple of 8: the workspace route
 ])
 def test_gemm_graph_replay_matches_eager(gemm_lib, M, N, K, cfg):

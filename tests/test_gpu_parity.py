@@ -17,7 +17,7 @@ from _gpu_util import check_against_oracle
 pytestmark = pytest.mark.gpu
 
 ALL_CFGS = [g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR,
-            g.TILE_128x128x64, g.TILE_128x128x64_SPLITK]
+            g.TILE_128x128x64, g.TILE_128x128x64_SPLITK, g.TILE_128x64x64]
 
 
 @pytest.mark.parametrize("w", inputs.WORKLOADS, ids=lambda w: w.name)
@@ -34,7 +34,7 @@ def test_workload_parity(gemm_lib, w):
 
 @pytest.mark.parametrize("w", [w for w in inputs.WORKLOADS if w.tile_cfg == 0], ids=lambda w: w.name)
 @pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR,
-                                 g.TILE_128x128x64, g.TILE_128x128x64_SPLITK])
+                                 g.TILE_128x128x64, g.TILE_128x128x64_SPLITK, g.TILE_128x64x64])
 def test_workload_parity_each_large_tile(gemm_lib, w, cfg):
     A, B = inputs.gemm_inputs(w.M, w.N, w.K, w.seed)
     C = g.gemm(A.cuda(), B.cuda(), group_size_m=w.group_size_m, tile_cfg=cfg)
@@ -58,6 +58,19 @@ EDGE_SHAPES = [
 def test_edge_shapes(gemm_lib, M, N, K, cfg):
     A, B = inputs.gemm_inputs(M, N, K, seed=M * 7 + N * 13 + K)
     C = g.gemm(A.cuda(), B.cuda(), group_size_m=3, tile_cfg=cfg)
+    assert g.query_status() == g.GEMM_OK
+    check_against_oracle(A, B, C)
+
+
+@pytest.mark.parametrize("cfg", ALL_CFGS)
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 8), (2000, 3000, 40), (8192, 1001, 8)])
+def test_many_short_tiles(gemm_lib, M, N, K, cfg):
+    # one k step per tile and many tiles per CTA: each tile's epilogue follows
+    # the previous one at once, so a staging buffer is refilled while the
+    # previous tile's store may still be reading it (N = 1001: the right-edge
+    # blocks are stored directly, between TMA stores of other tiles)
+    A, B = inputs.gemm_inputs(M, N, K, seed=M + N + K + 1)
+    C = g.gemm(A.cuda(), B.cuda(), tile_cfg=cfg)
     assert g.query_status() == g.GEMM_OK
     check_against_oracle(A, B, C)
 
@@ -332,8 +345,15 @@ def test_split_k_cluster(gemm_lib, M, N, K):
     A, B = inputs.gemm_inputs(M, N, K, seed=3 * M + N + K)
     plan = g.launch_plan(M, N, K, tile_cfg=g.TILE_128x128x64_SPLITK)
     tiles = -(-M // 128) * -(-N // 128)
+    k_tiles = -(-K // 64)
     assert plan["num_tiles"] == tiles
-    assert plan["grid_ctas"] % tiles == 0 or plan["grid_ctas"] <= tiles
+    assert plan["grid_ctas"] >= 1
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if k_tiles >= 2 and 2 * tiles <= sms:   # split: each CTA of a tile's cluster gets a k step
+        S = plan["grid_ctas"] // tiles
+        assert plan["grid_ctas"] == S * tiles and S in (2, 4, 8) and S <= k_tiles
+    else:              # nothing to split: the one-CTA 128 x 128 kernel, one CTA per tile
+        assert plan["grid_ctas"] == tiles
     C = g.gemm(A.cuda(), B.cuda(), tile_cfg=g.TILE_128x128x64_SPLITK)
     assert g.query_status() == g.GEMM_OK
     check_against_oracle(A, B, C)

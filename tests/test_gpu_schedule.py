@@ -64,6 +64,9 @@ def _kernel_trace(M, N, K, G, cfg, seed):
     (896, 192, 64, 2, g.TILE_128x64x32),
     (4095, 3000, 200, 4, g.TILE_128x128x64),
     (512, 640, 512, 2, g.TILE_128x128x64_SPLITK),   # 20 tiles, one cluster each
+    (1024, 768, 128, 2, g.TILE_128x64x64),     # the worked example's 96 tiles, 64-deep k steps
+    (4095, 3000, 200, 3, g.TILE_128x64x64),    # 32 x 47 tiles: several per CTA
+    (4095, 3000, 200, 3, g.TILE_128x64x32),    # the same with 32-deep k steps
 ])
 def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
     A, B, C, tr, TM, TN = _kernel_trace(M, N, K, G, cfg, seed=31)
