@@ -288,8 +288,9 @@ def run_ours(args, w, rank, world, local_rank):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    if g.query_status(dev) != g.GEMM_OK:
-        raise RuntimeError("device status after warm-up: " + g.status_string(g.GEMM_ERR_TIMEOUT))
+    st = g.query_status(dev)
+    if st != g.GEMM_OK:
+        raise RuntimeError("device status after warm-up: " + g.status_string(st))
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0).start() if rank == 0 else None
     if sampler is not None:
@@ -315,6 +316,8 @@ def run_ours(args, w, rank, world, local_rank):
     status = g.query_status(dev)
     if sampler is not None:
         sampler.stop()
+    if status != g.GEMM_OK:  # a kernel gave up on a wait: the timed work is incomplete
+        raise RuntimeError("device status after the timed steps: " + g.status_string(status))
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     if args.flush_l2:
         total_ms = sum(per_launch_ms)
