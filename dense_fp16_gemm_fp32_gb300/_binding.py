@@ -220,17 +220,23 @@ def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZ
         _check_operand(out, "out")
         if tuple(out.shape) != (M, N) or out.device != a.device:
             raise ValueError(f"out must be [{M},{N}] on {a.device}")
-    trace_ptr = None
-    if trace is not None:
-        if trace.dtype != torch.int32 or trace.device != a.device or not trace.is_contiguous():
-            raise ValueError("trace must be a contiguous int32 tensor on a's device")
-        trace_ptr = trace.data_ptr()
     lib = _lib if _lib is not None else load()
     pa, pb, pc = a.data_ptr(), b.data_ptr(), out.data_ptr()
     lda, ldb, ldc = _ld(a), _ld(b), _ld(out)
     args = (pa, lda, pb, ldb, pc, ldc, M, N, K)
     # operands that already suit the tensor maps need no workspace query
     tma_shaped = (pc | (pa | pb if K else 0)) & 15 == 0 and (ldc | (lda | ldb if K else 0)) & 7 == 0
+    trace_ptr = None
+    if trace is not None:
+        if trace.dtype != torch.int32 or trace.device != a.device or not trace.is_contiguous():
+            raise ValueError("trace must be a contiguous int32 tensor on a's device")
+        tm, tn, _ = tile_shape(tile_cfg, M, N, K)
+        tiles = -(-M // tm) * -(-N // tn)
+        if not tma_shaped and not repack:  # the generic-load kernel's 128 x 256 tiles
+            tiles = max(tiles, -(-M // 128) * -(-N // 256))
+        if trace.numel() < 3 * tiles:
+            raise ValueError(f"trace needs {3 * tiles} entries (3 per tile), got {trace.numel()}")
+        trace_ptr = trace.data_ptr()
     dev = a.device
     with _on_device(dev):
         need = ctypes.c_uint64(0)

@@ -133,7 +133,11 @@ int gemm_f16_f32acc(const void* A, const void* B, void* C, int64_t M, int64_t N,
  * and an optional tile trace.
  *
  *   tile_trace   NULL, or a device int32 array of 3 * num_tiles entries
- *                (num_tiles = ceil(M/TILE_M) * ceil(N/TILE_N)). When given,
+ *                (num_tiles = ceil(M/TILE_M) * ceil(N/TILE_N), the tile of
+ *                gemm_tile_shape; when the operands take the generic-load
+ *                kernel (gemm_f16_f32acc_strided), its 128 x 256 tile: size
+ *                the array for the larger count). The library cannot check
+ *                the array's size: a shorter one is written past its end. When given,
  *                the kernel's scheduler writes, for every pid it processes,
  *                tile_trace[3*pid + 0] = pid_m, [3*pid + 1] = pid_n,
  *                [3*pid + 2] = the CTA (blockIdx.x) that processed it, or for

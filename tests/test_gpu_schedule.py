@@ -97,3 +97,25 @@ def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
         assert grid <= sms * 4
     if M * N * K <= 1.3e10:
         check_against_oracle(A, B, C)
+
+
+def test_short_trace_is_refused_before_launch(gemm_lib):
+    # the kernels write 3 entries per tile: a shorter trace would be written past its end
+    A, B = inputs.gemm_inputs(512, 512, 64, seed=5)
+    a, b = A.cuda(), B.cuda()
+    n0 = g.launch_count()
+    short = torch.zeros(3 * 4 - 1, dtype=torch.int32, device="cuda")     # 4 pair tiles
+    with pytest.raises(ValueError):
+        g.gemm(a, b, tile_cfg=g.TILE_256x256x64_PAIR, trace=short)
+    # A one element off a 16-byte boundary without a workspace: the generic-load
+    # kernel's 128 x 256 tiles (8 here) need more entries than the 4 pair tiles
+    buf = torch.empty(a.numel() + 1, dtype=torch.float16, device="cuda")
+    buf[1:] = a.reshape(-1)
+    pair_sized = torch.zeros(3 * 4, dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        g.gemm(buf[1:].view(a.shape), b, tile_cfg=g.TILE_256x256x64_PAIR, trace=pair_sized, repack=False)
+    assert g.launch_count() == n0
+    full = torch.full((3 * 8,), -1, dtype=torch.int32, device="cuda")
+    g.gemm(buf[1:].view(a.shape), b, tile_cfg=g.TILE_256x256x64_PAIR, trace=full, repack=False)
+    assert g.query_status() == g.GEMM_OK
+    assert sorted((int(full[3 * i]), int(full[3 * i + 1])) for i in range(8)) == [(m, n) for m in range(4) for n in range(2)]
