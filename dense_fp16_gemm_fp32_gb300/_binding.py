@@ -402,10 +402,18 @@ def autotune(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
     Returns {"best": cfg, "us": {cfg: microseconds per launch}}."""
     _check_operand(a, "a")
     _check_operand(b, "b")
+    if a.device != b.device:
+        raise ValueError("a and b must be on the same device")
     M, K = a.shape
-    N = b.shape[1]
+    K2, N = b.shape
+    if K != K2:
+        raise ValueError(f"inner extents differ: a is {tuple(a.shape)}, b is {tuple(b.shape)}")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=a.device)
+    else:
+        _check_operand(out, "out")
+        if tuple(out.shape) != (M, N) or out.device != a.device:
+            raise ValueError(f"out must be [{M},{N}] on {a.device}")
     best = ctypes.c_int32(0)
     us = (ctypes.c_float * TILE_COUNT)()
     with _on_device(a.device):

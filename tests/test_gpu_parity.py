@@ -359,3 +359,16 @@ def test_split_k_cluster(gemm_lib, M, N, K):
     check_against_oracle(A, B, C)
     C2 = g.gemm(A.cuda(), B.cuda(), tile_cfg=g.TILE_128x128x64_SPLITK)
     assert torch.equal(C, C2)   # the partials are summed in a fixed order
+
+
+def test_autotune_checks_its_operands(gemm_lib):
+    a = torch.zeros((256, 128), dtype=torch.float16, device="cuda")
+    b = torch.zeros((128, 256), dtype=torch.float16, device="cuda")
+    n0 = g.launch_count()
+    with pytest.raises(ValueError):
+        g.autotune(a, b[:64], reps=1)                                   # inner extents differ
+    with pytest.raises(ValueError):
+        g.autotune(a, b, out=torch.empty((256, 128), dtype=torch.float16, device="cuda"), reps=1)
+    with pytest.raises(TypeError):
+        g.autotune(a, b, out=torch.empty((256, 256), dtype=torch.float32, device="cuda"), reps=1)
+    assert g.launch_count() == n0
