@@ -211,8 +211,11 @@ int32_t tuned_cfg(int64_t M, int64_t N, int64_t K)
 // tiles are bound by each CTA's operand loads (about 60 bytes per cycle into
 // one SM), so there the tile that spreads the loads over the most SMs wins:
 //  * few 128 x 128 tiles (at most kSplitKMaxTiles, a quarter of the SMs) with
-//    a long K (at least kSplitKMinK): split-K across a cluster
-//    (128x4096x4096: 10.1 us against 23.1 us for the one-CTA 128 x 256 tile);
+//    a long K (at least kSplitKMinK, or kSplitKNarrowMinK for one 128-row
+//    band): split-K across a cluster (128x4096x4096: 10.1 us against 23.1 us
+//    for the one-CTA 128 x 256 tile; 512x512x2048 6.7 against 8.1 for the pair
+//    tile; 128x4096x1536 6.4 against 8.2 for 128 x 64 x 64; with two or more
+//    bands at K = 1024 the pair tile is 4-7 % faster);
 //  * 128 x 64 tiles that fit one wave (kOneWave) with at most one 128-row band
 //    or K <= kSmallK: the one-CTA 128 x 64 x 64 tile (512^3 4.14 us against
 //    4.50 for the pair tile and 4.78 for 128 x 128; 1024x768x128 2.70 against
@@ -234,6 +237,7 @@ int32_t tuned_cfg(int64_t M, int64_t N, int64_t K)
 //    per unit of power at 8192^3, where both run power-capped).
 constexpr int64_t kSplitKMaxTiles = 38;
 constexpr int64_t kSplitKMinK = 2048;
+constexpr int64_t kSplitKNarrowMinK = 1024;
 constexpr int64_t kOneWave = 152;
 constexpr int64_t kSmallK = 512;
 constexpr int64_t kOnePairWave = 76;
@@ -245,7 +249,8 @@ int auto_cfg(int64_t M, int64_t N, int64_t K)
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     const int64_t small_tiles = ((M + 127) / 128) * ((N + 127) / 128);
     const int64_t narrow_tiles = ((M + 127) / 128) * ((N + 63) / 64);
-    if (small_tiles <= kSplitKMaxTiles && K >= kSplitKMinK) return GEMM_TILE_128x128x64_SPLITK;
+    if (small_tiles <= kSplitKMaxTiles && (K >= kSplitKMinK || (M <= 128 && K >= kSplitKNarrowMinK)))
+        return GEMM_TILE_128x128x64_SPLITK;
     if (narrow_tiles <= kOneWave && (M <= 128 || K <= kSmallK)) return GEMM_TILE_128x64x64;
     if (M <= 128) return GEMM_TILE_128x256x64;
     if (2 * pair_tiles <= kOnePairWave) return K > kSmallK ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x128x64;
@@ -505,13 +510,21 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     return GEMM_OK;
 }
 
-// K-split factor for 128 x 128 tiles: the largest power of two up to the
-// portable cluster size that gives every CTA at least one k step and keeps
-// tiles x S within one CTA per SM.
+// K-split factor for 128 x 128 tiles: the largest of 2, 4 and 8 that gives
+// every CTA at least one k step, keeps tiles x S within one CTA per SM, and
+// uses eight-CTA clusters for at most kSplitK8MaxCtas CTAs. Measured (CUDA
+// graphs): with 4 or 8 tiles S = 8 is fastest (256x256x8192 8.9 us against
+// 12.4 for S = 4), with 16 tiles sixteen eight-CTA clusters run about twice
+// as long as S = 4 (512x512x4096 13.4 against 8.9 us; 512x512x2048 11.3
+// against 6.7), and S = 4 beats S = 2 on every shape measured.
+constexpr int64_t kSplitK8MaxCtas = 64;
+
 int splitk_factor(int64_t tiles, int64_t k_tiles, int64_t sm_count)
 {
     int s = 1;
-    while (s < kMaxSplitK && 2 * s <= k_tiles && tiles * 2 * s <= sm_count) s *= 2;
+    while (s < kMaxSplitK && 2 * s <= k_tiles && tiles * 2 * s <= sm_count &&
+           (2 * s < 8 || tiles * 2 * s <= kSplitK8MaxCtas))
+        s *= 2;
     return s;
 }
 

@@ -77,7 +77,8 @@ typedef enum {
 typedef enum {
     GEMM_TILE_AUTO = 0,       /* the library picks: the configuration gemm_autotune chose for
                                  this (M, N, K) on the current device; else 128x128x64_SPLITK
-                                 when there are at most 38 tiles of 128x128 and K >= 2048;
+                                 when there are at most 38 tiles of 128x128 and K >= 2048
+                                 (K >= 1024 when M <= 128);
                                  128x64x64 when its tiles fit one wave (at most 152) and
                                  M <= 128 or K <= 512; 128x256x64 when M <= 128; with at most
                                  38 tiles of 256x256 (every one split into column halves),
@@ -95,9 +96,10 @@ typedef enum {
                                  problems with few tiles */
     GEMM_TILE_128x128x64_SPLITK = 6, /* a cluster of S = 2, 4 or 8 CTAs per 128x128 tile, each
                                  running 1/S of the k steps; the fp32 partials are summed
-                                 through distributed shared memory (S: the largest power of
-                                 two <= 8 with S <= ceil(K/64) and tiles * S <= SMs; S = 1
-                                 runs the 128x128x64 kernel) */
+                                 through distributed shared memory (S: the largest of 2, 4
+                                 and 8 with S <= ceil(K/64), tiles * S <= SMs, and
+                                 tiles * S <= 64 for S = 8; S = 1 runs the 128x128x64
+                                 kernel) */
     GEMM_TILE_128x64x64 = 7,  /* 1 CTA per tile, 8 stages of 64-deep k steps: four times the
                                  tiles of 128x256 and A rows of 128 bytes, for problems whose
                                  time is each CTA's operand loads */

@@ -39,7 +39,9 @@ def test_status_strings(lib):
 
 
 def test_tile_shapes(lib):
-    assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=1024) == (128, 64, 64)     # one band, 64 tiles of 128x64
+    assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=512) == (128, 64, 64)      # one band, 64 tiles of 128x64
+    assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=1024) == (128, 128, 64)    # one band, 32 tiles: split-K
+    assert g.tile_shape(g.TILE_AUTO, M=256, N=2048, K=1024) == (256, 256, 128)   # two bands at K = 1024: pair
     assert g.tile_shape(g.TILE_AUTO, M=128, N=16384, K=1024) == (128, 256, 64)   # one band, 256 tiles of 128x64
     assert g.tile_shape(g.TILE_AUTO, M=129, N=8192, K=1024) == (256, 256, 128)   # 32 pair tiles: all split
     assert g.tile_shape(g.TILE_AUTO, M=129, N=10240, K=1024) == (128, 256, 64)   # 40 pair tiles: under one wave

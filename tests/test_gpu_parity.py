@@ -333,27 +333,22 @@ def test_autotune_picks_fastest_and_auto_follows(gemm_lib):
     assert g.tile_shape(g.TILE_AUTO, M, N, K) == default_shape
 
 
-@pytest.mark.parametrize("M,N,K", [
-    (512, 512, 512),      # 16 tiles x 8-way split
-    (1024, 768, 128),     # 2 k steps: 2-way
-    (300, 257, 320),      # 5 k steps over a 4-CTA cluster: the last CTA has none (a zero partial)
-    (129, 1000, 4000),    # ragged M and N, long K
-    (1, 8, 8),
-    (100, 100, 64),       # a single k step: no split
+@pytest.mark.parametrize("M,N,K,S", [
+    (512, 512, 512, 4),       # 16 tiles: eight-CTA clusters only up to 64 CTAs
+    (1024, 768, 128, 2),      # 2 k steps: 2-way
+    (300, 257, 320, 4),       # 5 k steps over a 4-CTA cluster: the last CTA has none (a zero partial)
+    (129, 1000, 4000, 4),     # ragged M and N, long K, 16 tiles
+    (300, 200, 4096, 8),      # 6 tiles: 48 CTAs in eight-CTA clusters
+    (1, 8, 8, 1),
+    (100, 100, 64, 1),        # a single k step: no split
 ])
-def test_split_k_cluster(gemm_lib, M, N, K):
+def test_split_k_cluster(gemm_lib, M, N, K, S):
     A, B = inputs.gemm_inputs(M, N, K, seed=3 * M + N + K)
     plan = g.launch_plan(M, N, K, tile_cfg=g.TILE_128x128x64_SPLITK)
     tiles = -(-M // 128) * -(-N // 128)
-    k_tiles = -(-K // 64)
     assert plan["num_tiles"] == tiles
-    assert plan["grid_ctas"] >= 1
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    if k_tiles >= 2 and 2 * tiles <= sms:   # split: each CTA of a tile's cluster gets a k step
-        S = plan["grid_ctas"] // tiles
-        assert plan["grid_ctas"] == S * tiles and S in (2, 4, 8) and S <= k_tiles
-    else:              # nothing to split: the one-CTA 128 x 128 kernel, one CTA per tile
-        assert plan["grid_ctas"] == tiles
+    # one cluster of S CTAs per tile; S = 1 is the one-CTA 128 x 128 kernel
+    assert plan["grid_ctas"] == S * tiles
     C = g.gemm(A.cuda(), B.cuda(), tile_cfg=g.TILE_128x128x64_SPLITK)
     assert g.query_status() == g.GEMM_OK
     check_against_oracle(A, B, C)
