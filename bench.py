@@ -361,7 +361,7 @@ def run_ours(args, w, rank, world, local_rank):
         "clocks": clocks,
         "device_status": g.status_string(status),
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the oracle's timing: one process, rank 0, N = 1
         line["cpu_baseline"] = cpu_baseline(A, B, w.seed, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     return 0
@@ -579,7 +579,7 @@ def run_softmax(args, w, rank, world, local_rank):
         "gpu_launches": launches,
         "clocks": sampler.summary(t_host0, t_host1) if sampler is not None else None,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the oracle's timing: one process, rank 0, N = 1
         line["cpu_baseline"] = softmax_cpu_baseline(X.numpy(), w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     return 0
