@@ -13,13 +13,23 @@ the host and copied to the device before timing). Rank 0 prints one JSON line.
   (--flush-l2 adds one between steps, outside the timed events).
 * roofline: the GEMM kernel's average launch duration from per-launch CUDA
   events, 2*M*N*K flops per launch, against the measured dense bf16 tensor
-  peak (fp16 runs at the bf16 rate) from MEASURED_PEAKS.json; traffic is the
+  rate (fp16 runs at the bf16 rate) from MEASURED_PEAKS.json; traffic is the
   DRAM bytes per launch from the committed ncu summary for this kernel
   source, or null when the kernel changed since that capture.
+* sustained: after the timed steps, a second timed region of back-to-back
+  launches lasting at least --sustained-s seconds (default 2.5), long enough
+  for the power cap to settle; its TFLOP/s, the median SM clock of the
+  clock samples taken under load inside it, TFLOP/s per GHz and the fraction
+  of the measured sustained bf16 rate. The timed steps of `value` are a burst
+  when they last less than the power cap's settling time.
+* pct_of_peak: the kernel's rate against NVIDIA's published dense fp16/bf16
+  tensor-core rate of one GB300 (2.25 PFLOP/s: 36 PFLOP/s per 8 GPUs with
+  2:4 sparsity, halved); roofline.frac is against the measured rate.
 * e2e: the same metric end to end from pinned host memory: per step the
   host-to-device copies of A and B, the GEMM, and the device-to-host copy of C.
 * cpu_baseline: the CPU oracle on a bounded, seeded sample of rows of the
-  same workload, timed on this host's cores (rank 0 only).
+  same workload, timed on this host's cores (rank 0 only), plus a
+  single-thread rate on a smaller sample and the host's CPU model.
 * --impl reference: the oracle alone as the reference arm, on the host.
 * --workload softmax_<M>x<n>: the fused row softmax instead (GB/s of 8 bytes
   per element, roofline against the measured HBM copy bandwidth).
@@ -46,6 +56,11 @@ METRIC = "fp16 GEMM TFLOP/s (fp32 acc) at M=N=K=8192; % of GB300 dense fp16 TC p
 UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# NVIDIA's published dense fp16/bf16 tensor-core rate of one GB300 (HGX B300:
+# 36 PFLOP/s FP16/BF16 per 8 GPUs with 2:4 structured sparsity; dense is half)
+NOMINAL_F16_TFLOPS = 2250.0
+NOMINAL_F16_SOURCE = ("NVIDIA HGX B300 specification: 36 PFLOP/s FP16/BF16 tensor per 8 GPUs with 2:4 "
+                      "sparsity, i.e. 2.25 PFLOP/s dense per GPU")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -144,9 +159,18 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self, t0: float, t1: float):
+    def idle_power(self, before: float):
+        """Lowest power drawn in the samples taken before host time `before` (None if none)."""
+        pw = [s[3] for s in self.samples if s[0] < before and s[3] is not None]
+        return min(pw) if pw else None
+
+    def summary(self, t0: float, t1: float, idle_w=None):
+        """Clocks over the samples inside [t0, t1]. Under-load samples are those
+        drawing more than a quarter of the way from the idle power (before the
+        region) to the region's peak power; sm_mhz_under_load is their median."""
         inside = [s for s in self.samples if t0 <= s[0] <= t1]
         window = "timed region"
+        n_inside = len(inside)
         if not inside and self.samples:
             mid = 0.5 * (t0 + t1)
             inside = sorted(self.samples, key=lambda s: abs(s[0] - mid))[:3]
@@ -155,9 +179,16 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "no samples"}
         reasons = sorted({r for s in inside for r in s[4]})
         pw = [s[3] for s in inside if s[3] is not None]
-        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
-                "reasons": reasons, "power_w_max": max(pw) if pw else None, "samples": len(inside),
-                "window": window}
+        out = {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+               "reasons": reasons, "power_w_max": max(pw) if pw else None, "samples": n_inside,
+               "window": window, "seconds": t1 - t0, "period_ms": self.period_ms}
+        if n_inside and pw and idle_w is not None:
+            cut = idle_w + 0.25 * (max(pw) - idle_w)
+            loaded = [s for s in inside if s[3] is not None and s[3] > cut]
+            out["idle_w"] = idle_w
+            out["samples_under_load"] = len(loaded)
+            out["sm_mhz_under_load"] = statistics.median(s[1] for s in loaded) if loaded else None
+        return out
 
 
 # ---------------------------------------------------------------- ranks
@@ -186,9 +217,46 @@ def time_oracle(A, B, rows, nthreads):
     return time.perf_counter() - t
 
 
-def cpu_baseline(A, B, seed: int, target_s: float):
-    """The oracle as it stands on a seeded sample of rows: ~target_s of work."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def oracle_rate(A, B, perm, threads: int, target_s: float):
+    """(TFLOP/s, rows, seconds) of the oracle on about target_s of seeded rows."""
     import numpy as np
+
+    M, K = A.shape
+    N = B.shape[1]
+    # two calibration runs separate the per-call cost (B converted to fp32 once
+    # per call) from the per-row cost
+    calib = min(M, max(threads, 4))
+    t1 = time_oracle(A, B, np.sort(perm[:calib]), threads)
+    t2 = time_oracle(A, B, np.sort(perm[:2 * calib]), threads) if 2 * calib <= M else 2 * t1
+    per_row = max((t2 - t1) / calib, 1e-6)
+    fixed = max(t1 - calib * per_row, 0.0)
+    n = int(min(M, max(calib, (target_s - fixed) / per_row)))
+    t = time_oracle(A, B, np.sort(perm[:n]), threads)
+    return 2.0 * n * N * K / t / 1e12, n, t
+
+
+def cpu_baseline(A, B, seed: int, target_s: float, single_s: float = 4.0):
+    """The oracle as it stands on a seeded sample of rows: ~target_s of work on
+    every core of this process's affinity, then ~single_s on one thread."""
     import torch
     from oracle import gemm as og
 
@@ -197,20 +265,13 @@ def cpu_baseline(A, B, seed: int, target_s: float):
     cores = og.default_threads()
     g = torch.Generator().manual_seed(seed + 2000)
     perm = torch.randperm(M, generator=g).numpy()
-    # two calibration runs separate the per-call cost (B converted to fp32 once
-    # per call) from the per-row cost
-    calib = min(M, max(cores, 4))
-    t1 = time_oracle(A, B, np.sort(perm[:calib]), cores)
-    t2 = time_oracle(A, B, np.sort(perm[:2 * calib]), cores) if 2 * calib <= M else 2 * t1
-    per_row = max((t2 - t1) / calib, 1e-6)
-    fixed = max(t1 - calib * per_row, 0.0)
-    n = int(min(M, max(calib, (target_s - fixed) / per_row)))
-    rows = np.sort(perm[:n])
-    t = time_oracle(A, B, rows, cores)
-    flops = 2.0 * n * N * K
-    return {"value": flops / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+    value, n, t = oracle_rate(A, B, perm, cores, target_s)
+    v1, n1, t1 = oracle_rate(A, B, perm, 1, single_s)
+    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{n} seeded rows of the {M}x{N}x{K} workload ({n * N} outputs), "
-                      f"{t:.1f} s, fp32 ascending-k C loop with {cores} threads"}
+                      f"{t:.1f} s, fp32 ascending-k C loop with {cores} threads",
+            "single_thread": {"value": v1, "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} seeded rows of the same workload, {t1:.1f} s, one thread"}}
 
 
 # ---------------------------------------------------------------- arms
@@ -314,9 +375,9 @@ def run_ours(args, w, rank, world, local_rank):
         dist.barrier()
     launches = g.launch_count() - n_launch0
     status = g.query_status(dev)
-    if sampler is not None:
-        sampler.stop()
     if status != g.GEMM_OK:  # a kernel gave up on a wait: the timed work is incomplete
+        if sampler is not None:
+            sampler.stop()
         raise RuntimeError("device status after the timed steps: " + g.status_string(status))
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     if args.flush_l2:
@@ -325,7 +386,31 @@ def run_ours(args, w, rank, world, local_rank):
         total_ms = starts[0].elapsed_time(ends[-1])
     total_ms_max = max_over_ranks(total_ms, dev, world)
 
+    # ---- a seconds-long region of back-to-back launches: the power-capped rate
+    sustained = None
+    if args.sustained_s > 0 and not args.flush_l2:
+        # at most 20000 launches: below ~0.1 ms per launch the region is host-bound anyway
+        n_sus = max(1, min(20000, int(args.sustained_s / max(statistics.fmean(per_launch_ms) * 1e-3, 1e-6))))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_launch1 = g.launch_count()
+        t_sus0 = time.time()
+        e0.record(stream)
+        for _ in range(n_sus):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_sus1 = time.time()
+        sus_launches = g.launch_count() - n_launch1
+        st = g.query_status(dev)
+        if st != g.GEMM_OK:
+            raise RuntimeError("device status after the sustained region: " + g.status_string(st))
+        sustained = {"steps": n_sus, "ms": e0.elapsed_time(e1), "launches": sus_launches,
+                     "t0": t_sus0, "t1": t_sus1}
+
     # ---- end to end through the public API from pinned host buffers
+    if sampler is not None:
+        time.sleep(0.2)  # samples after the sustained region's end
+        sampler.stop()
     e2e_ms, e2e_steps, e2e_mode = run_e2e(args, w, g, A, B, dev, world)
 
     if rank != 0:
@@ -337,23 +422,42 @@ def run_ours(args, w, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    clocks = sampler.summary(t_host0, t_host1) if sampler is not None else None
+    idle_w = sampler.idle_power(t_host0) if sampler is not None else None
+    clocks = sampler.summary(t_host0, t_host1, idle_w) if sampler is not None else None
+    sus_line = None
+    if sustained is not None:
+        sus_tflops = flops * sustained["steps"] / (sustained["ms"] * 1e-3) / 1e12
+        sus_clocks = sampler.summary(sustained["t0"], sustained["t1"], idle_w) if sampler is not None else None
+        mhz = sus_clocks.get("sm_mhz_under_load") if sus_clocks else None
+        sus_line = {"value": sus_tflops, "unit": UNIT, "seconds": sustained["ms"] * 1e-3,
+                    "steps": sustained["steps"], "gpu_launches": sustained["launches"],
+                    "sm_mhz_under_load": mhz,
+                    "tflops_per_ghz": sus_tflops / (mhz * 1e-3) if mhz else None,
+                    "peak_sustained": peak_sustained, "frac_sustained": sus_tflops / peak_sustained,
+                    "peak_sustained_source": f"{peak_src} bf16 GEMM back to back for seconds under the power "
+                                             "cap (bf16_tflops_sustained, MEASURED_PEAKS.json)",
+                    "pct_of_nominal_peak": 100.0 * sus_tflops / NOMINAL_F16_TFLOPS,
+                    "clocks": sus_clocks}
+    main_s = (t_host1 - t_host0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": config_dict(w, args, tile),
-        "pct_of_peak": 100.0 * achieved / peak,
+        "pct_of_peak": 100.0 * achieved / NOMINAL_F16_TFLOPS,
+        "nominal_peak": {"value": NOMINAL_F16_TFLOPS, "unit": UNIT, "source": NOMINAL_F16_SOURCE},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": load_traffic(f"{w.name}/{tile}/G{args.group_size_m}"),
-                     "peak_source": f"{peak_src} dense bf16 burst (bf16_tflops, MEASURED_PEAKS.json); "
-                                    "fp16 and bf16 share the tensor rate",
-                     "peak_sustained": peak_sustained, "frac_sustained": achieved / peak_sustained,
-                     "peak_sustained_source": f"{peak_src} bf16 GEMM back to back for seconds under the power cap "
-                                              "(bf16_tflops_sustained): the like-for-like figure for this "
-                                              "timed region of back-to-back launches",
+                     "peak_source": f"{peak_src} dense bf16 rate of cuBLAS in a burst (bf16_tflops, "
+                                    "MEASURED_PEAKS.json), the reference for a kernel timed alone; fp16 and bf16 "
+                                    "share the tensor rate",
+                     "timed_region_s": main_s,
+                     "regime": ("burst: the timed steps last less than the power cap's settling time; "
+                                "the sustained key holds the power-capped rate")
+                               if main_s < 1.0 else "seconds-long timed region",
                      "kernel": f"{kernel_name} {tile}", "kernel_ms": kernel_ms,
                      "flops_per_launch": flops},
+        "sustained": sus_line,
         "e2e": {"value": whole_job_tflops(flops, e2e_steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": 2 * (w.M * w.K + w.K * w.N), "d2h_bytes_per_step": 2 * w.M * w.N,
                 "steps": e2e_steps, "mode": e2e_mode},
@@ -600,6 +704,8 @@ def main():
                    help="device and pinned host buffer sets the end-to-end leg rotates through")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--sustained-s", type=float, default=2.5,
+                   help="seconds of back-to-back launches timed after the steps (0: none)")
     p.add_argument("--reference-budget-s", type=float, default=90.0)
     args = p.parse_args()
     if args.warmup < 3:

@@ -612,10 +612,11 @@ int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 
 // ---------------------------------------------------------------- no-alloc variant
 // Scratch for gemm_f16_f32acc_noalloc. Some callers may not allocate device
-// memory at the moment they run a GEMM: code being captured into a CUDA graph
-// (cudaMalloc is refused during capture), plugin hooks of inference runtimes
-// whose enqueue step forbids allocation, or runtimes that hand out all device
-// memory through their own allocator. The default entry point allocates its
+// memory at the moment they run a GEMM: plugin hooks of inference runtimes
+// whose enqueue step forbids allocation, runtimes that reserve all device
+// memory up front and hand it out through their own allocator, and
+// latency-critical loops in which the implicit synchronisation of a
+// cudaMalloc is not acceptable. The default entry point allocates its
 // 4-byte status word with cudaMalloc on its first call on a device; this
 // variant keeps that word in the array below instead, so it never allocates.
 // Word 0 is the status word of the call in flight; the rest is headroom.
@@ -1071,7 +1072,7 @@ int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, in
     p.status = d->scratch;  // word 0 of the static scratch array
     p.trace = nullptr;
     p.watchdog_ns = watchdog_ns();
-    p.fault_mode = 0;
+    p.fault_mode = g_fault_mode.load();  // the watchdog test hook reaches this entry point too
     p.num_full_tiles = p.num_tiles;
     p.num_units = p.num_tiles;
     p.A = p.B = nullptr;

@@ -325,10 +325,10 @@ uint64_t gemm_launch_count(void);
  * gemm_f16_f32acc_noalloc -- the same GEMM as gemm_f16_f32acc, run with the
  * one-CTA 128x256x64 tile, for callers that cannot allocate device memory when they
  * call it. The pages have no counterpart to this entry point: it exists for
- * callers such as code being captured into a CUDA graph (cudaMalloc is
- * refused during capture), inference-runtime plugins whose enqueue step must
- * not allocate, or hosts whose device memory is owned by their own allocator.
- * gemm_f16_f32acc allocates its 4-byte status word with cudaMalloc on its
+ * callers such as inference-runtime plugins whose enqueue step must not
+ * allocate, hosts that reserve all device memory up front and own it through
+ * their own allocator, and latency-critical loops that cannot take the
+ * implicit synchronisation of a cudaMalloc. gemm_f16_f32acc allocates its 4-byte status word with cudaMalloc on its
  * first call on a device; this entry point calls no cudaMalloc, cudaFree or
  * allocating library routine. Its only scratch is a file-scope device array
  * of 256 bytes (64 32-bit words, one word used: the watchdog status word),
@@ -340,8 +340,14 @@ uint64_t gemm_launch_count(void);
  *              16-byte aligned, N or K not a multiple of 8) give
  *              GEMM_ERR_UNSUPPORTED: this entry point has no generic kernel
  *   d_status   NULL, or a device uint32_t that receives, in stream order after
- *              the kernel, this call's status word: 0 = complete, bit 0 set =
- *              a bounded wait expired (the output is then incomplete)
+ *              the kernel, this call's raw status word: 0 = complete; bit 0
+ *              set = a bounded wait expired (the output is then incomplete),
+ *              and bits 8..15 then name the role whose wait expired first
+ *              (1 TMA producer, 2 MMA issuer, 3 epilogue, 4 drain after an
+ *              abort; several CTAs may OR in different roles). Test bit 0,
+ *              not equality with 1. The watchdog limit and the test hook of
+ *              gemm_set_watchdog_ns and gemm_set_fault_injection apply here
+ *              as to every other entry point.
  *
  * The first call on a device (with that device current) looks up the
  * scratch array's device address (cudaGetSymbolAddress) and sets the

@@ -71,10 +71,19 @@ def test_device_pointer_errors(gemm_lib):
     # C aliasing A
     rc = lib.gemm_f16_f32acc(a.data_ptr(), b.data_ptr(), a.data_ptr(), 64, 64, 64, 8, s)
     assert rc == g.GEMM_ERR_INVALID_ARG
-    # C at a 2-byte offset, K = 60: the generic-load kernel runs them
+    # C at a 2-byte offset: the generic-load kernel writes it; the elements
+    # before and after C keep their values
+    A, B = inputs.gemm_inputs(64, 64, 64, seed=43)
+    a, b = A.cuda(), B.cuda()
+    c.fill_(float("nan"))
     rc = lib.gemm_f16_f32acc(a.data_ptr(), b.data_ptr(), c.data_ptr() + 2, 64, 64, 64, 8, s)
     assert rc == g.GEMM_OK
-    g.gemm(a[:, :60].contiguous(), b[:60].contiguous())
+    assert g.query_status() == g.GEMM_OK
+    assert torch.isnan(c[0]) and torch.isnan(c[64 * 64 + 1:]).all()
+    check_against_oracle(A, B, c[1:1 + 64 * 64].view(64, 64))
+    # K = 60 (rows of 120 bytes): the generic-load kernel as well
+    A, B = inputs.gemm_inputs(64, 64, 60, seed=44)
+    check_against_oracle(A, B, g.gemm(A.cuda(), B.cuda()))
     assert g.query_status() == g.GEMM_OK
 
 
