@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     TILE_128x256x64,
     TILE_256x256x64_PAIR,
     TILE_256x256x128_PAIR,
+    TILE_256x256x128_PAIR_ALIGNED,
     TILE_AUTO,
     TILE_COUNT,
     GemmError,

@@ -29,7 +29,8 @@ TILE_256x256x128_PAIR = 4
 TILE_128x128x64 = 5
 TILE_128x128x64_SPLITK = 6
 TILE_128x64x64 = 7
-TILE_COUNT = 8
+TILE_256x256x128_PAIR_ALIGNED = 8
+TILE_COUNT = 9
 
 DEFAULT_GROUP_SIZE_M = 8
 
@@ -140,6 +141,23 @@ def _stream_ptr(device: torch.device):
     return torch.cuda.current_stream(device).cuda_stream
 
 
+# The current stream's handle and the current device as plain ints, read from
+# torch's C layer without building Python Stream/device objects (a few
+# microseconds per call otherwise); the public calls when these are absent.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_raw_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
+def _stream_of(index: int) -> int:
+    if _raw_stream is not None:
+        return int(_raw_stream(index))
+    return torch.cuda.current_stream(index).cuda_stream
+
+
+def _current_device() -> int:
+    return int(_raw_device()) if _raw_device is not None else torch.cuda.current_device()
+
+
 class _Nothing:
     def __enter__(self):
         return None
@@ -188,6 +206,28 @@ def _ld(t: torch.Tensor) -> int:
     return max(8, -(-int(t.shape[1]) // 8) * 8)
 
 
+def _matrix(t, name: str, dtype=torch.float16):
+    """(rows, cols, data pointer, row pitch, device index) of a 2-D row-major
+    CUDA matrix, with the checks of _check_operand in one pass."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {str(dtype).replace('torch.', '')}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device, got {t.device}")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(t.shape)}")
+    rows, cols = t.shape
+    s0, s1 = t.stride()
+    if rows > 1 and cols > 1:
+        if s1 != 1 or s0 < cols:
+            raise ValueError(f"{name} must be row-major: unit column stride and a row stride >= its columns")
+    elif not (t.is_contiguous() or s1 == 1 or cols <= 1):
+        raise ValueError(f"{name} must be row-major: unit column stride and a row stride >= its columns")
+    ld = int(s0) if rows > 1 else max(8, -(-int(cols) // 8) * 8)
+    return rows, cols, t.data_ptr(), ld, t.get_device()
+
+
 def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZE_M,
          out: torch.Tensor | None = None, tile_cfg: int = TILE_AUTO,
          trace: torch.Tensor | None = None, repack: bool = True) -> torch.Tensor:
@@ -206,23 +246,20 @@ def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZ
     (pid_m, pid_n, cta) per program id, as the kernel's scheduler ran them.
     Runs on the current CUDA stream of a's device.
     """
-    _check_operand(a, "a")
-    _check_operand(b, "b")
-    if a.device != b.device:
+    M, K, pa, lda, dev_a = _matrix(a, "a")
+    K2, N, pb, ldb, dev_b = _matrix(b, "b")
+    if dev_a != dev_b:
         raise ValueError("a and b must be on the same device")
-    M, K = a.shape
-    K2, N = b.shape
     if K != K2:
         raise ValueError(f"inner extents differ: a is {tuple(a.shape)}, b is {tuple(b.shape)}")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=a.device)
+        pc, ldc = out.data_ptr(), (N if M > 1 else max(8, -(-N // 8) * 8))
     else:
-        _check_operand(out, "out")
-        if tuple(out.shape) != (M, N) or out.device != a.device:
+        Mo, No, pc, ldc, dev_c = _matrix(out, "out")
+        if (Mo, No) != (M, N) or dev_c != dev_a:
             raise ValueError(f"out must be [{M},{N}] on {a.device}")
     lib = _lib if _lib is not None else load()
-    pa, pb, pc = a.data_ptr(), b.data_ptr(), out.data_ptr()
-    lda, ldb, ldc = _ld(a), _ld(b), _ld(out)
     args = (pa, lda, pb, ldb, pc, ldc, M, N, K)
     # operands that already suit the tensor maps need no workspace query
     tma_shaped = (pc | (pa | pb if K else 0)) & 15 == 0 and (ldc | (lda | ldb if K else 0)) & 7 == 0
@@ -237,12 +274,17 @@ def gemm(a: torch.Tensor, b: torch.Tensor, group_size_m: int = DEFAULT_GROUP_SIZ
         if trace.numel() < 3 * tiles:
             raise ValueError(f"trace needs {3 * tiles} entries (3 per tile), got {trace.numel()}")
         trace_ptr = trace.data_ptr()
+    if tma_shaped and dev_a == _current_device():  # the common case: no workspace, no device switch
+        rc = lib.gemm_f16_f32acc_strided(*args, int(group_size_m), int(tile_cfg), trace_ptr, _stream_of(dev_a))
+        if rc != GEMM_OK:
+            raise GemmError(rc, "gemm_f16_f32acc_strided")
+        return out
     dev = a.device
     with _on_device(dev):
         need = ctypes.c_uint64(0)
         if repack and not tma_shaped:
             _check(lib.gemm_workspace_bytes(*args, ctypes.byref(need)), "gemm_workspace_bytes")
-        stream = torch.cuda.current_stream(dev).cuda_stream
+        stream = _stream_of(dev_a)
         if need.value:
             ws = torch.empty(need.value, dtype=torch.uint8, device=dev)  # caching allocator: stream-ordered reuse
             rc = lib.gemm_f16_f32acc_strided_ws(*args, int(group_size_m), int(tile_cfg), trace_ptr, ws.data_ptr(),
@@ -399,7 +441,9 @@ def autotune(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
              group_size_m: int = DEFAULT_GROUP_SIZE_M, reps: int = 20) -> dict:
     """Times every tile configuration on a @ b (out is overwritten) and makes
     the fastest the TILE_AUTO choice for this shape on this device.
-    Returns {"best": cfg, "us": {cfg: microseconds per launch}}."""
+    Returns {"best": cfg, "us": {cfg: microseconds per launch}} (configurations
+    that do not apply to the shape, such as the aligned one on partial tiles,
+    are left out)."""
     _check_operand(a, "a")
     _check_operand(b, "b")
     if a.device != b.device:
@@ -421,7 +465,7 @@ def autotune(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
                                   int(group_size_m), int(reps), ctypes.byref(best), us,
                                   _stream_ptr(a.device))
     _check(rc, "gemm_autotune")
-    return {"best": best.value, "us": {c: float(us[c]) for c in range(1, TILE_COUNT)}}
+    return {"best": best.value, "us": {c: float(us[c]) for c in range(1, TILE_COUNT) if us[c] >= 0}}
 
 
 def autotune_clear() -> None:

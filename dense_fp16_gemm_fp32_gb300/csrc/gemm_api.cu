@@ -26,31 +26,32 @@ using Cfg128x128 = TileCfg<128, 128, 64, 6>;
 using CfgSplitK = TileCfg<128, 128, 64, 4>;  // the ring also holds the 64 KiB fp32 partial tile
 using Cfg128x64x64 = TileCfg<128, 64, 64, 8>;
 using CfgGeneric = TileCfg<128, 256, 64, 4, true>;  // plain loads and stores (operands TMA cannot address)
-constexpr int kGenericCfgId = 8;
+constexpr int kGenericCfgId = 15;  // per-device launch state slot of the generic-load kernel
 constexpr int kMaxSplitK = 8;  // portable cluster size
 using CfgPair256 = PairCfg<6>;
 using CfgPair256Deep = PairCfg<3, 128>;
+using CfgPair256Aligned = PairCfg<3, 128, true>;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumCfgs = 9;  // the tile configurations 1..7 and the generic-load kernel
+constexpr int kNumCfgs = 16;  // launch state slots: the tile configurations and the generic-load kernel
 constexpr int64_t kMaxExtent = int64_t(1) << 30;
 constexpr uint64_t kDefaultWatchdogNs = 2000000000ull;
 
 struct DeviceState {
-    bool ready = false;
+    std::atomic<bool> ready{false};  // set once, after the fields below (read without the lock)
     int sm_count = 0;
     uint32_t* status = nullptr;  // one word, cudaMalloc'd on first use
-    bool attr_set[kNumCfgs] = {};
+    std::atomic<bool> attr_set[kNumCfgs] = {};  // per configuration: set once, after ctas_per_sm
     int ctas_per_sm[kNumCfgs] = {};
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
-EncodeTiledFn g_encode = nullptr;
+std::atomic<EncodeTiledFn> g_encode{nullptr};
 std::atomic<int> g_last_cuda_error{0};
 std::atomic<uint64_t> g_watchdog_ns{0};
 std::atomic<int> g_fault_mode{0};
@@ -74,25 +75,28 @@ uint64_t watchdog_ns()
     return kDefaultWatchdogNs;
 }
 
-// Per-device state; allocates the status word on the first call.
+// Per-device state; allocates the status word on the first call. After
+// that, a call reads the state without taking the lock.
 int device_state(DeviceState** out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mu);
     DeviceState& d = g_dev[dev];
-    if (!d.ready) {
-        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return cuda_fail(e);
-        if (d.status == nullptr) {
-            e = cudaMalloc(&d.status, sizeof(uint32_t));
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return cuda_fail(e);
-            e = cudaMemset(d.status, 0, sizeof(uint32_t));
-            if (e != cudaSuccess) return cuda_fail(e);
+            if (d.status == nullptr) {
+                e = cudaMalloc(&d.status, sizeof(uint32_t));
+                if (e != cudaSuccess) return cuda_fail(e);
+                e = cudaMemset(d.status, 0, sizeof(uint32_t));
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+            d.ready.store(true, std::memory_order_release);
         }
-        d.ready = true;
     }
     *out = &d;
     return GEMM_OK;
@@ -100,17 +104,51 @@ int device_state(DeviceState** out)
 
 int encode_fn(EncodeTiledFn* fn)
 {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_encode == nullptr) {
+    EncodeTiledFn f = g_encode.load(std::memory_order_acquire);
+    if (f == nullptr) {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
         cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
         if (e != cudaSuccess) return cuda_fail(e);
         if (q != cudaDriverEntryPointSuccess || p == nullptr) return cuda_fail(cudaErrorSymbolNotFound);
-        g_encode = reinterpret_cast<EncodeTiledFn>(p);
+        f = reinterpret_cast<EncodeTiledFn>(p);
+        g_encode.store(f, std::memory_order_release);  // every thread resolves the same entry point
     }
-    *fn = g_encode;
+    *fn = f;
     return GEMM_OK;
+}
+
+// Encoded tensor maps of the calling thread's recent calls. A map is a pure
+// function of its arguments (base address, extents, pitch, box, swizzle), so
+// a call that repeats them copies the 128-byte map instead of encoding it
+// again (measured about a microsecond per GEMM call for the three or four
+// maps of a launch). Direct-mapped, per thread: no lock.
+struct MapKey {
+    const void* base;
+    uint64_t inner, outer, pitch;
+    uint32_t box_inner, box_outer;
+    int32_t swz;
+    bool operator==(const MapKey& o) const
+    {
+        return base == o.base && inner == o.inner && outer == o.outer && pitch == o.pitch &&
+               box_inner == o.box_inner && box_outer == o.box_outer && swz == o.swz;
+    }
+};
+struct MapSlot {
+    bool valid = false;
+    MapKey key{};
+    CUtensorMap map;
+};
+constexpr int kMapSlots = 32;
+thread_local MapSlot t_maps[kMapSlots];
+
+int map_slot(const MapKey& k)
+{
+    uint64_t h = reinterpret_cast<uintptr_t>(k.base) >> 4;
+    h ^= k.inner * 0x9E3779B97F4A7C15ull;
+    h ^= (k.outer + (static_cast<uint64_t>(k.box_inner) << 32)) * 0xC2B2AE3D27D4EB4Full;
+    h ^= (k.pitch + k.box_outer + (static_cast<uint64_t>(k.swz) << 20)) * 0x165667B19E3779F9ull;
+    return static_cast<int>((h ^ (h >> 29)) % kMapSlots);
 }
 
 // 2-D fp16 tensor map: `inner` contiguous elements per row, `outer` rows,
@@ -118,6 +156,12 @@ int encode_fn(EncodeTiledFn* fn)
 int make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz)
 {
+    const MapKey key{base, inner, outer, pitch_elems, box_inner, box_outer, static_cast<int32_t>(swz)};
+    MapSlot& slot = t_maps[map_slot(key)];
+    if (slot.valid && slot.key == key) {
+        *map = slot.map;
+        return GEMM_OK;
+    }
     EncodeTiledFn fn = nullptr;
     int rc = encode_fn(&fn);
     if (rc != GEMM_OK) return rc;
@@ -129,6 +173,9 @@ int make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    slot.key = key;
+    slot.map = *map;
+    slot.valid = true;
     return GEMM_OK;
 }
 
@@ -286,9 +333,19 @@ int resolve_cfg(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tm, 
         case GEMM_TILE_128x64x64:
             *tm = Cfg128x64x64::TM, *tn = Cfg128x64x64::TN, *tk = Cfg128x64x64::TK;
             return GEMM_TILE_128x64x64;
+        case GEMM_TILE_256x256x128_PAIR_ALIGNED:
+            *tm = CfgPair256Aligned::TM, *tn = CfgPair256Aligned::TN, *tk = CfgPair256Aligned::TK;
+            return GEMM_TILE_256x256x128_PAIR_ALIGNED;
         default:
             return -1;
     }
+}
+
+// The aligned configuration's promise: every extent a whole number of its tiles.
+bool whole_tiles(int cfg, int64_t M, int64_t N, int64_t K)
+{
+    if (cfg != GEMM_TILE_256x256x128_PAIR_ALIGNED) return true;
+    return M % CfgPair256Aligned::TM == 0 && N % CfgPair256Aligned::TN == 0 && K % CfgPair256Aligned::TK == 0;
 }
 
 #ifndef GEMM_PDL
@@ -315,9 +372,9 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     int rc = device_state(&d);
     if (rc != GEMM_OK) return rc;
     auto kernel = gemm_f16_f32acc_kernel<Cfg>;
-    {
+    if (!d->attr_set[cfg_id].load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!d->attr_set[cfg_id]) {
+        if (!d->attr_set[cfg_id].load(std::memory_order_relaxed)) {
             cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
             if (e != cudaSuccess) return cuda_fail(e);
             int occ = 0;
@@ -325,7 +382,7 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
             if (e != cudaSuccess) return cuda_fail(e);
             const int tmem_fit = static_cast<int>(512u / Cfg::TMEM_COLS);
             d->ctas_per_sm[cfg_id] = occ < 1 ? 1 : (occ < tmem_fit ? occ : tmem_fit);
-            d->attr_set[cfg_id] = true;
+            d->attr_set[cfg_id].store(true, std::memory_order_release);
         }
     }
 
@@ -416,8 +473,12 @@ template <class Cfg>
 int pair_clusters(DeviceState* d, int cfg_id, int64_t* clusters)
 {
     auto kernel = gemm_f16_f32acc_pair_kernel<Cfg>;
+    if (d->attr_set[cfg_id].load(std::memory_order_acquire)) {
+        *clusters = d->ctas_per_sm[cfg_id];
+        return GEMM_OK;
+    }
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!d->attr_set[cfg_id]) {
+    if (!d->attr_set[cfg_id].load(std::memory_order_relaxed)) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
         cudaLaunchAttribute attr = pair_cluster_attr();
@@ -431,7 +492,7 @@ int pair_clusters(DeviceState* d, int cfg_id, int64_t* clusters)
         e = cudaOccupancyMaxActiveClusters(&n, kernel, &q);
         if (e != cudaSuccess) return cuda_fail(e);
         d->ctas_per_sm[cfg_id] = n < 1 ? 1 : n;  // for pair configurations: resident clusters per device
-        d->attr_set[cfg_id] = true;
+        d->attr_set[cfg_id].store(true, std::memory_order_release);
     }
     *clusters = d->ctas_per_sm[cfg_id];
     return GEMM_OK;
@@ -544,16 +605,16 @@ int launch_splitk(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t st
     if (S == 1) return launch<Cfg128x128>(pr, GEMM_TILE_128x128x64, trace, stream);
     auto kernel = S == 2 ? gemm_f16_f32acc_splitk_kernel<Cfg, 2>
                 : S == 4 ? gemm_f16_f32acc_splitk_kernel<Cfg, 4> : gemm_f16_f32acc_splitk_kernel<Cfg, 8>;
-    {
+    if (!d->attr_set[cfg_id].load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!d->attr_set[cfg_id]) {
+        if (!d->attr_set[cfg_id].load(std::memory_order_relaxed)) {
             for (auto k : {gemm_f16_f32acc_splitk_kernel<Cfg, 2>, gemm_f16_f32acc_splitk_kernel<Cfg, 4>,
                            gemm_f16_f32acc_splitk_kernel<Cfg, 8>}) {
                 const cudaError_t e =
                     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
                 if (e != cudaSuccess) return cuda_fail(e);
             }
-            d->attr_set[cfg_id] = true;
+            d->attr_set[cfg_id].store(true, std::memory_order_release);
         }
     }
     CUtensorMap ma, mb;
@@ -730,6 +791,8 @@ int dispatch_tma(const Problem& pr, int cfg, int32_t* trace, cudaStream_t s)
             return launch_splitk(pr, cfg, trace, s);
         case GEMM_TILE_128x64x64:
             return launch<Cfg128x64x64>(pr, cfg, trace, s);
+        case GEMM_TILE_256x256x128_PAIR_ALIGNED:
+            return launch_pair<CfgPair256Aligned>(pr, cfg, trace, s);
         default:
             return launch<Cfg128x256>(pr, cfg, trace, s);
     }
@@ -761,12 +824,15 @@ int gemm_f16_f32acc_strided_ws(const void* A, int64_t lda, const void* B, int64_
     if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
     int rc = validate(pr);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    if (!whole_tiles(cfg, M, N, K)) return GEMM_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (tma_ok(pr)) return dispatch_tma(pr, cfg, tile_trace, s);
     const WsLayout w = ws_layout(pr);
     const uintptr_t ws = reinterpret_cast<uintptr_t>(workspace);
-    if (workspace == nullptr || workspace_bytes < w.bytes || (ws & (kWsAlign - 1)) != 0)
+    if (workspace == nullptr || workspace_bytes < w.bytes || (ws & (kWsAlign - 1)) != 0) {
+        if (cfg == GEMM_TILE_256x256x128_PAIR_ALIGNED) return GEMM_ERR_UNSUPPORTED;  // a TMA kernel only
         return launch<CfgGeneric>(pr, kGenericCfgId, tile_trace, s);
+    }
     // the workspace must not overlap an operand
     using u128 = unsigned __int128;
     const u128 ws_end = static_cast<u128>(ws) + w.bytes;
@@ -807,8 +873,12 @@ int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t l
     if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
     int rc = validate(pr);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    if (!whole_tiles(cfg, M, N, K)) return GEMM_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (!tma_ok(pr)) return launch<CfgGeneric>(pr, kGenericCfgId, tile_trace, s);
+    if (!tma_ok(pr)) {
+        if (cfg == GEMM_TILE_256x256x128_PAIR_ALIGNED) return GEMM_ERR_UNSUPPORTED;  // a TMA kernel only
+        return launch<CfgGeneric>(pr, kGenericCfgId, tile_trace, s);
+    }
     return dispatch_tma(pr, cfg, tile_trace, s);
 }
 
@@ -848,6 +918,10 @@ int gemm_autotune(const void* A, int64_t lda, const void* B, int64_t ldb, void* 
     int32_t best = -1;
     float best_us = 0.f;
     for (int32_t cfg = 1; cfg < GEMM_TILE_COUNT && rc == GEMM_OK; ++cfg) {
+        if (!whole_tiles(cfg, M, N, K)) {  // the aligned configuration does not apply: not timed
+            if (us_per_cfg != nullptr) us_per_cfg[cfg] = -1.f;
+            continue;
+        }
         for (int i = 0; i < 2 && rc == GEMM_OK; ++i) rc = dispatch_tma(pr, cfg, nullptr, s);  // warm-up
         if (rc != GEMM_OK) break;
         if ((e = cudaEventRecord(ev[0], s)) != cudaSuccess) rc = cuda_fail(e);
@@ -911,10 +985,12 @@ int gemm_launch_plan(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t*
     int rc = device_state(&d);
     if (rc != GEMM_OK) return rc;
     int64_t ctas = 0, split = 0;
-    if (cfg == GEMM_TILE_256x256x64_PAIR || cfg == GEMM_TILE_256x256x128_PAIR) {
+    if (cfg == GEMM_TILE_256x256x64_PAIR || cfg == GEMM_TILE_256x256x128_PAIR ||
+        cfg == GEMM_TILE_256x256x128_PAIR_ALIGNED) {
         int64_t clusters = 0;
-        rc = cfg == GEMM_TILE_256x256x64_PAIR ? pair_clusters<CfgPair256>(d, cfg, &clusters)
-                                              : pair_clusters<CfgPair256Deep>(d, cfg, &clusters);
+        rc = cfg == GEMM_TILE_256x256x64_PAIR    ? pair_clusters<CfgPair256>(d, cfg, &clusters)
+             : cfg == GEMM_TILE_256x256x128_PAIR ? pair_clusters<CfgPair256Deep>(d, cfg, &clusters)
+                                                 : pair_clusters<CfgPair256Aligned>(d, cfg, &clusters);
         if (rc != GEMM_OK) return rc;
         split = split_tail_tiles(tiles, clusters);
         const int64_t units = tiles + split;
@@ -926,7 +1002,8 @@ int gemm_launch_plan(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t*
         // one-CTA kernels (an unsplit split-K problem runs the 128 x 128 one);
         // occupancy is set up on first launch: until then report the SM bound
         const int occ_id = cfg == GEMM_TILE_128x128x64_SPLITK ? GEMM_TILE_128x128x64 : cfg;
-        const int per_sm = d->attr_set[occ_id] && d->ctas_per_sm[occ_id] > 0 ? d->ctas_per_sm[occ_id] : 1;
+        const int per_sm = d->attr_set[occ_id].load(std::memory_order_acquire) && d->ctas_per_sm[occ_id] > 0
+                               ? d->ctas_per_sm[occ_id] : 1;
         const int64_t slots = static_cast<int64_t>(d->sm_count) * per_sm;
         ctas = tiles < slots ? tiles : slots;
     }

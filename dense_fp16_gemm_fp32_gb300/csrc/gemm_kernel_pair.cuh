@@ -48,9 +48,15 @@ namespace gemm103 {
 // stored as TK/64 sub-tiles of 128 rows x 64 k (one 128-byte swizzle span per
 // row); its B panel as CTA_N/64 boxes of TK k rows x 64 columns. Deeper stages
 // amortise the per-stage wait, fence and commits over more MMAs.
-template <int STAGES_, int TK_ = 64>
+// ALIGNED: the aligned specialisation of "03: Matrix multiplication" (the
+// @ph.aligned contract: every extent a whole number of tiles, so no masks).
+// The host launches it only when M and N are multiples of 256 and K of TK;
+// the epilogue's edge tests are then compiled out (loads need none: a TMA box
+// never reaches past the tensor when the extents are whole tiles).
+template <int STAGES_, int TK_ = 64, bool ALIGNED_ = false>
 struct PairCfg {
     static constexpr int TM = 256, TN = 256, TK = TK_, STAGES = STAGES_;  // tile of the pair
+    static constexpr bool ALIGNED = ALIGNED_;
     static_assert(TK == 64 || TK == 128, "stage depth of 64 or 128");
     static constexpr int CTA_M = 128;                                     // A / D rows per CTA
     static constexpr int CTA_N = 128;                                     // B columns per CTA
@@ -346,22 +352,23 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             };
             const int32_t c_row0 = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + q * 32;
             uint8_t* staging = sC + (warp - 2) * EpiStaging<Cfg::EPI_COLS_LAST>::WARP_BYTES;
+            constexpr bool kA = Cfg::ALIGNED;
             if (u + num_pairs < p.num_units && p.K > Cfg::WIDE_EPI_MAX_K) {
                 if (un.half < 0)
-                    epilogue_tma_store<Cfg::TN, Cfg::EPI_COLS>(t_row, staging, &tmap_c, c_row0, n0, p.M, p.N, p.C, p.ldc,
-                                                               lane, release);
+                    epilogue_tma_store<Cfg::TN, Cfg::EPI_COLS, false, kA>(t_row, staging, &tmap_c, c_row0, n0, p.M,
+                                                                          p.N, p.C, p.ldc, lane, release);
                 else
-                    epilogue_tma_store<Cfg::TN / 2, Cfg::EPI_COLS>(t_row, staging, &tmap_c, c_row0, n0, p.M, p.N, p.C,
-                                                                   p.ldc, lane, release);
+                    epilogue_tma_store<Cfg::TN / 2, Cfg::EPI_COLS, false, kA>(t_row, staging, &tmap_c, c_row0, n0,
+                                                                              p.M, p.N, p.C, p.ldc, lane, release);
             } else {  // 64-column buffers overlap the 32-column ones: drain earlier stores first
                 if (lane == 0) bulk_wait_group_read<0>();
                 __syncwarp();
                 if (un.half < 0)
-                    epilogue_tma_store<Cfg::TN, Cfg::EPI_COLS_LAST>(t_row, staging, &tmap_c_last, c_row0, n0, p.M, p.N,
-                                                                    p.C, p.ldc, lane, release);
+                    epilogue_tma_store<Cfg::TN, Cfg::EPI_COLS_LAST, false, kA>(t_row, staging, &tmap_c_last, c_row0,
+                                                                               n0, p.M, p.N, p.C, p.ldc, lane, release);
                 else
-                    epilogue_tma_store<Cfg::TN / 2, Cfg::EPI_COLS_LAST>(t_row, staging, &tmap_c_last, c_row0, n0, p.M,
-                                                                        p.N, p.C, p.ldc, lane, release);
+                    epilogue_tma_store<Cfg::TN / 2, Cfg::EPI_COLS_LAST, false, kA>(
+                        t_row, staging, &tmap_c_last, c_row0, n0, p.M, p.N, p.C, p.ldc, lane, release);
             }
             if (++buf == 2) {
                 buf = 0;

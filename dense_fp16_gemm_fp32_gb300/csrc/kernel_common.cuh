@@ -151,7 +151,10 @@ struct EpiStaging {
 // base or pitch is not one a TMA store can address). Direct stores are the
 // slower form even where nothing overlaps the epilogue (measured: each lane
 // owns a row, so a warp's 16-byte stores touch 32 cache lines at once).
-template <int TN, int COLS, bool kDirect = false, class Release>
+// kAligned: the caller guarantees that the tile lies wholly inside C (M and N
+// whole multiples of the tile), so the edge tests are compiled out and every
+// block is one TMA store.
+template <int TN, int COLS, bool kDirect = false, bool kAligned = false, class Release>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* staging, const CUtensorMap* tmap_c,
                                                    int32_t c_row0, int32_t n0, int32_t M, int32_t N,
                                                    uint16_t* C, int64_t ldc, int lane, Release release)
@@ -181,7 +184,8 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
             for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r0[2 * i], r0[2 * i + 1]);
         }
         const int32_t x = n0 + c * COLS;
-        if (kDirect || ((N & 7) != 0 && x + COLS > N)) {  // or right edge inside a 16-byte granule
+        static_assert(!(kDirect && kAligned), "the aligned form stores through TMA");
+        if (kDirect || (!kAligned && (N & 7) != 0 && x + COLS > N)) {  // or right edge inside a 16-byte granule
             const int32_t row = c_row0 + lane;
             if (row < M && x < N) {
                 uint16_t* dst = C + static_cast<int64_t>(row) * ldc + x;
@@ -221,7 +225,7 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if (c_row0 < M && x < N) tma_store_2d(tmap_c, staging + (c & 1) * St::BUF_BYTES, x, c_row0);
+            if (kAligned || (c_row0 < M && x < N)) tma_store_2d(tmap_c, staging + (c & 1) * St::BUF_BYTES, x, c_row0);
             bulk_commit_group();  // an empty group keeps the per-buffer accounting uniform
         }
     }

@@ -103,7 +103,15 @@ typedef enum {
     GEMM_TILE_128x64x64 = 7,  /* 1 CTA per tile, 8 stages of 64-deep k steps: four times the
                                  tiles of 128x256 and A rows of 128 bytes, for problems whose
                                  time is each CTA's operand loads */
-    GEMM_TILE_COUNT = 8       /* number of values above, GEMM_TILE_AUTO included */
+    GEMM_TILE_256x256x128_PAIR_ALIGNED = 8, /* the aligned, mask-free form of 4 ("03: Matrix
+                                 multiplication", the @ph.aligned decorator and the paragraph
+                                 under its listing): the caller promises that M and N are
+                                 multiples of 256 and K of 128, and the kernel carries no edge
+                                 tests. Any other extents give GEMM_ERR_UNSUPPORTED, as do
+                                 operands a tensor map cannot describe when no workspace is
+                                 given. Never chosen by GEMM_TILE_AUTO (4 computes the same
+                                 bits); gemm_autotune times it only on whole tiles */
+    GEMM_TILE_COUNT = 9       /* number of values above, GEMM_TILE_AUTO included */
 } gemm_tile_cfg_t;
 
 /*
@@ -188,7 +196,9 @@ int gemm_f16_f32acc_strided(const void* A, int64_t lda, const void* B, int64_t l
  *              launches), timed with CUDA events on `stream`
  *   best_cfg   host int32, or NULL: the chosen configuration
  *   us_per_cfg host array of GEMM_TILE_COUNT floats, or NULL: [c] = mean
- *              microseconds per launch of configuration c, [0] = the best
+ *              microseconds per launch of configuration c (-1 for the
+ *              aligned configuration when the extents are not whole tiles:
+ *              not timed), [0] = the best
  *
  * Synchronous (waits for its events): not for use under stream capture.
  * gemm_autotune_clear() forgets every choice.

@@ -61,6 +61,8 @@ def _kernel_trace(M, N, K, G, cfg, seed):
     (8192, 8192, 256, 8, g.TILE_256x256x128_PAIR),
     (512, 1024, 256, 2, g.TILE_256x256x128_PAIR),    # 8 tiles: every tile split
     (2048, 4096, 256, 3, g.TILE_256x256x128_PAIR),
+    (2048, 4096, 256, 3, g.TILE_256x256x128_PAIR_ALIGNED),
+    (8192, 8192, 256, 8, g.TILE_256x256x128_PAIR_ALIGNED),
     (896, 192, 64, 2, g.TILE_128x64x32),
     (4095, 3000, 200, 4, g.TILE_128x128x64),
     (512, 640, 512, 2, g.TILE_128x128x64_SPLITK),   # 20 tiles, one cluster each
@@ -77,7 +79,7 @@ def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
     plan = g.launch_plan(M, N, K, tile_cfg=cfg)
     assert plan["num_tiles"] == len(want)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    if cfg in (g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR):
+    if cfg in (g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR, g.TILE_256x256x128_PAIR_ALIGNED):
         clusters = plan["grid_ctas"] // 2
         assert 1 <= clusters <= sms // 2
         split = plan["split_tiles"]
