@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     TILE_256x256x64_PAIR,
     TILE_256x256x128_PAIR,
     TILE_256x256x128_PAIR_ALIGNED,
+    TILE_256x256x64_PAIR_STREAMK,
     TILE_AUTO,
     TILE_COUNT,
     GemmError,
@@ -43,6 +44,7 @@ from ._binding import (  # noqa: F401
     softmax_launch_count,
     softmax_plan,
     status_string,
+    tile_config,
     tile_map_host,
     tile_schedule,
     tile_shape,

@@ -30,7 +30,8 @@ TILE_128x128x64 = 5
 TILE_128x128x64_SPLITK = 6
 TILE_128x64x64 = 7
 TILE_256x256x128_PAIR_ALIGNED = 8
-TILE_COUNT = 9
+TILE_256x256x64_PAIR_STREAMK = 9
+TILE_COUNT = 10
 
 DEFAULT_GROUP_SIZE_M = 8
 
@@ -58,6 +59,7 @@ _SIGNATURES = {
                                                ctypes.c_int32, ctypes.c_int32, _c_void_p, _c_void_p]),
     "gemm_tile_shape": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                        _c_void_p, _c_void_p, _c_void_p]),
+    "gemm_tile_config": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _c_void_p]),
     "gemm_tile_schedule": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_int32, _c_void_p, _c_void_p, _c_void_p]),
     "gemm_tile_map_host": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
@@ -301,6 +303,13 @@ def tile_shape(tile_cfg: int = TILE_AUTO, M: int = 0, N: int = 0, K: int = 0) ->
     _check(load().gemm_tile_shape(int(tile_cfg), M, N, K, ctypes.byref(tm), ctypes.byref(tn), ctypes.byref(tk)),
            "gemm_tile_shape")
     return tm.value, tn.value, tk.value
+
+
+def tile_config(tile_cfg: int = TILE_AUTO, M: int = 0, N: int = 0, K: int = 0) -> int:
+    """The configuration tile_cfg resolves to for (M, N, K) (TILE_AUTO: the tuned or rule choice)."""
+    r = ctypes.c_int32()
+    _check(load().gemm_tile_config(int(tile_cfg), M, N, K, ctypes.byref(r)), "gemm_tile_config")
+    return r.value
 
 
 def launch_plan(M: int, N: int, K: int = 0, tile_cfg: int = TILE_AUTO, device=None) -> dict:

@@ -31,6 +31,7 @@ constexpr int kMaxSplitK = 8;  // portable cluster size
 using CfgPair256 = PairCfg<6>;
 using CfgPair256Deep = PairCfg<3, 128>;
 using CfgPair256Aligned = PairCfg<3, 128, true>;
+using CfgPair256StreamK = PairCfg<6, 64, false, true>;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -290,6 +291,17 @@ constexpr int64_t kSmallK = 512;
 constexpr int64_t kOnePairWave = 76;
 constexpr int64_t kShortK = 256;
 constexpr int64_t kDeepK = 4096;
+// Stream-K pays only where its partial sums are small next to a tile's k
+// loop: the fp32 partial of a shared tile is written and read back through
+// the SMs' operand path, which is what bounds these kernels, so each shared
+// tile costs about 256 KiB per SM against KT x 32 KiB of operands. Measured
+// (CUDA graphs, one GB300): 4096x3072x8192 114.96 us against 119.46 for the
+// 64-deep and 122.23 for the 128-deep pair tile, 4096x3072x4096 57.92
+// against 58.84, but 4095x3000x2000 37.34 against 36.52, the ragged
+// 4095x3000x1000 26.28 against 24.95 and 3072x3072x512 13.75 against 8.94.
+// Beyond a few waves the last wave's share of the time is too small to win.
+constexpr int64_t kStreamKMinK = 4096;
+constexpr int64_t kStreamKMaxWaves = 8;
 
 int auto_cfg(int64_t M, int64_t N, int64_t K)
 {
@@ -302,6 +314,9 @@ int auto_cfg(int64_t M, int64_t N, int64_t K)
     if (M <= 128) return GEMM_TILE_128x256x64;
     if (2 * pair_tiles <= kOnePairWave) return K > kSmallK ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x128x64;
     if (pair_tiles < kOnePairWave || K <= kShortK) return GEMM_TILE_128x256x64;
+    if (K >= kStreamKMinK && 2 * (pair_tiles % kOnePairWave) > kOnePairWave &&
+        pair_tiles <= kStreamKMaxWaves * kOnePairWave)
+        return GEMM_TILE_256x256x64_PAIR_STREAMK;
     return K <= kDeepK ? GEMM_TILE_256x256x64_PAIR : GEMM_TILE_256x256x128_PAIR;
 }
 
@@ -336,6 +351,9 @@ int resolve_cfg(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tm, 
         case GEMM_TILE_256x256x128_PAIR_ALIGNED:
             *tm = CfgPair256Aligned::TM, *tn = CfgPair256Aligned::TN, *tk = CfgPair256Aligned::TK;
             return GEMM_TILE_256x256x128_PAIR_ALIGNED;
+        case GEMM_TILE_256x256x64_PAIR_STREAMK:
+            *tm = CfgPair256StreamK::TM, *tn = CfgPair256StreamK::TN, *tk = CfgPair256StreamK::TK;
+            return GEMM_TILE_256x256x64_PAIR_STREAMK;
         default:
             return -1;
     }
@@ -430,6 +448,10 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     p.B = static_cast<const uint16_t*>(pr.B);
     p.lda = pr.lda;
     p.ldb = pr.ldb;
+    p.sk_first_tile = p.num_tiles;
+    p.sk_iters = 0;
+    p.sk_ws = nullptr;
+    p.sk_flags = nullptr;
 
     const int64_t slots = static_cast<int64_t>(d->sm_count) * d->ctas_per_sm[cfg_id];
     const unsigned grid = static_cast<unsigned>(num_tiles < slots ? num_tiles : slots);
@@ -498,10 +520,21 @@ int pair_clusters(DeviceState* d, int cfg_id, int64_t* clusters)
     return GEMM_OK;
 }
 
+// The stream-K schedule of one launch (gemm_kernel_pair.cuh): the whole
+// tiles below first_tile, `iters` (tile, k step) iterations split over the
+// clusters, and the workspace the tails' partial sums go through.
+struct SkPlan {
+    int32_t first_tile;
+    int32_t iters;
+    float* ws;
+    uint32_t* flags;
+};
+
 // Cluster launch of the CTA-pair kernel: one 2-CTA cluster per 256 x 256 tile
-// slot, as many clusters as can be resident at once (persistent).
+// slot, as many clusters as can be resident at once (persistent). A stream-K
+// configuration needs its plan (sk), computed for exactly those clusters.
 template <class Cfg>
-int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
+int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream, const SkPlan* sk = nullptr)
 {
     DeviceState* d = nullptr;
     int rc = device_state(&d);
@@ -552,11 +585,27 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     p.fault_mode = g_fault_mode.load();
     p.A = p.B = nullptr;  // the pair kernel loads through its tensor maps
     p.lda = p.ldb = 0;
+    p.sk_first_tile = p.num_tiles;
+    p.sk_iters = 0;
+    p.sk_ws = nullptr;
+    p.sk_flags = nullptr;
 
-    const int64_t split = split_tail_tiles(num_tiles, slots);
-    p.num_full_tiles = static_cast<int32_t>(num_tiles - split);
-    p.num_units = static_cast<int32_t>(num_tiles + split);
-    const int64_t pairs = p.num_units < slots ? p.num_units : slots;
+    int64_t pairs = 0;
+    if constexpr (Cfg::STREAMK) {
+        if (sk == nullptr) return GEMM_ERR_UNSUPPORTED;
+        p.sk_first_tile = sk->first_tile;
+        p.sk_iters = sk->iters;
+        p.sk_ws = sk->ws;
+        p.sk_flags = sk->flags;
+        p.num_full_tiles = p.num_tiles;
+        p.num_units = p.num_tiles;
+        pairs = slots;  // the plan splits the iterations over exactly these clusters
+    } else {
+        const int64_t split = split_tail_tiles(num_tiles, slots);
+        p.num_full_tiles = static_cast<int32_t>(num_tiles - split);
+        p.num_units = static_cast<int32_t>(num_tiles + split);
+        pairs = p.num_units < slots ? p.num_units : slots;
+    }
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     lc.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
@@ -569,6 +618,127 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
     if (e != cudaSuccess) return cuda_fail(e);
     g_launches.fetch_add(1);
     return GEMM_OK;
+}
+
+// ---------------------------------------------------------------- stream-K
+// Tiles of a stream-K launch on `clusters` resident clusters, or 0 when the
+// plain pair schedule is used instead: stream-K when there is at least one
+// full wave and the last partial wave holds more than half of the clusters
+// (at most half: the split tail halves it without any partial sums). The
+// last partial wave plus one full wave are split by k iterations, so every
+// cluster's range holds at least one tile's k steps.
+int64_t streamk_tiles(int64_t tiles, int64_t k_tiles, int64_t clusters)
+{
+    if (clusters <= 0 || k_tiles <= 0 || tiles < clusters) return 0;
+    const int64_t rem = tiles % clusters;
+    if (2 * rem <= clusters) return 0;
+    const int64_t sk = rem + clusters;
+    if (sk * k_tiles > INT32_MAX) return 0;
+    return sk;
+}
+
+// Stream-K workspace of one stream on one device: partial tiles and flags for
+// up to 2 x clusters stream-K tiles, allocated on the first stream-K launch on
+// that stream and kept until the process exits. Launches on one stream run in
+// order, so they can share it; launches on different streams get different
+// workspaces. Flags start (and are left) at zero.
+constexpr int kMaxSkSpaces = 64;
+constexpr size_t kSkTileFloats = 256u * 256u;  // one fp32 partial tile
+constexpr size_t kSkTileFlags = 2u * 4u;       // per CTA of the pair and epilogue warp
+
+struct SkSpace {
+    int dev = -1;
+    cudaStream_t stream = nullptr;
+    int64_t slots = 0;
+    float* ws = nullptr;
+    uint32_t* flags = nullptr;
+};
+std::mutex g_sk_mu;
+SkSpace g_sk[kMaxSkSpaces];
+int g_sk_count = 0;
+
+// The workspace for (current device, stream) with room for `slots` tiles.
+// GEMM_ERR_UNSUPPORTED when none exists and one cannot be made now (the
+// stream is being captured, or the table is full): the caller then runs the
+// plain schedule.
+int sk_space(int dev, cudaStream_t s, int64_t slots, SkSpace** out)
+{
+    std::lock_guard<std::mutex> lock(g_sk_mu);
+    for (int i = 0; i < g_sk_count; ++i) {
+        if (g_sk[i].dev == dev && g_sk[i].stream == s && g_sk[i].slots >= slots) {
+            *out = &g_sk[i];
+            return GEMM_OK;
+        }
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (cs != cudaStreamCaptureStatusNone || g_sk_count == kMaxSkSpaces) return GEMM_ERR_UNSUPPORTED;
+    SkSpace sp;
+    sp.dev = dev;
+    sp.stream = s;
+    sp.slots = slots;
+    e = cudaMalloc(&sp.ws, static_cast<size_t>(slots) * kSkTileFloats * sizeof(float));
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaMalloc(&sp.flags, static_cast<size_t>(slots) * kSkTileFlags * sizeof(uint32_t));
+    if (e != cudaSuccess) {
+        cudaFree(sp.ws);
+        return cuda_fail(e);
+    }
+    e = cudaMemset(sp.flags, 0, static_cast<size_t>(slots) * kSkTileFlags * sizeof(uint32_t));
+    if (e != cudaSuccess) {
+        cudaFree(sp.ws);
+        cudaFree(sp.flags);
+        return cuda_fail(e);
+    }
+    g_sk[g_sk_count] = sp;
+    *out = &g_sk[g_sk_count++];
+    return GEMM_OK;
+}
+
+// Clears the flags of every stream-K workspace of a device (after a timeout,
+// an aborted launch may have left a flag raised).
+int sk_clear_flags(int dev)
+{
+    std::lock_guard<std::mutex> lock(g_sk_mu);
+    for (int i = 0; i < g_sk_count; ++i) {
+        if (g_sk[i].dev != dev) continue;
+        const cudaError_t e =
+            cudaMemset(g_sk[i].flags, 0, static_cast<size_t>(g_sk[i].slots) * kSkTileFlags * sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return GEMM_OK;
+}
+
+// GEMM_TILE_256x256x64_PAIR_STREAMK: the stream-K pair kernel where the
+// schedule applies and a workspace is at hand, the plain 64-deep pair kernel
+// (with its split tail) otherwise.
+int launch_streamk(const Problem& pr, int32_t* trace, cudaStream_t stream)
+{
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != GEMM_OK) return rc;
+    int64_t clusters = 0;
+    rc = pair_clusters<CfgPair256StreamK>(d, GEMM_TILE_256x256x64_PAIR_STREAMK, &clusters);
+    if (rc != GEMM_OK) return rc;
+    using Cfg = CfgPair256StreamK;
+    const int64_t tiles = ((pr.M + Cfg::TM - 1) / Cfg::TM) * ((pr.N + Cfg::TN - 1) / Cfg::TN);
+    const int64_t k_tiles = (pr.K + Cfg::TK - 1) / Cfg::TK;
+    const int64_t sk_tiles = streamk_tiles(tiles, k_tiles, clusters);
+    if (sk_tiles > 0 && tiles <= INT32_MAX) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        SkSpace* sp = nullptr;
+        rc = sk_space(dev, stream, 2 * clusters, &sp);
+        if (rc == GEMM_OK) {
+            const SkPlan plan{static_cast<int32_t>(tiles - sk_tiles), static_cast<int32_t>(sk_tiles * k_tiles), sp->ws,
+                              sp->flags};
+            return launch_pair<Cfg>(pr, GEMM_TILE_256x256x64_PAIR_STREAMK, trace, stream, &plan);
+        }
+        if (rc != GEMM_ERR_UNSUPPORTED) return rc;
+    }
+    return launch_pair<CfgPair256>(pr, GEMM_TILE_256x256x64_PAIR, trace, stream);
 }
 
 // K-split factor for 128 x 128 tiles: the largest of 2, 4 and 8 that gives
@@ -643,6 +813,10 @@ int launch_splitk(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t st
     p.num_units = p.num_tiles;
     p.A = p.B = nullptr;
     p.lda = p.ldb = 0;
+    p.sk_first_tile = p.num_tiles;
+    p.sk_iters = 0;
+    p.sk_ws = nullptr;
+    p.sk_flags = nullptr;
 
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -793,6 +967,8 @@ int dispatch_tma(const Problem& pr, int cfg, int32_t* trace, cudaStream_t s)
             return launch<Cfg128x64x64>(pr, cfg, trace, s);
         case GEMM_TILE_256x256x128_PAIR_ALIGNED:
             return launch_pair<CfgPair256Aligned>(pr, cfg, trace, s);
+        case GEMM_TILE_256x256x64_PAIR_STREAMK:
+            return launch_streamk(pr, trace, s);
         default:
             return launch<Cfg128x256>(pr, cfg, trace, s);
     }
@@ -972,6 +1148,15 @@ int gemm_tile_shape(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* 
     return GEMM_OK;
 }
 
+int gemm_tile_config(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* resolved)
+{
+    int32_t tm, tn, tk;
+    const int cfg = resolve_cfg(tile_cfg, M, N, K, &tm, &tn, &tk);
+    if (cfg < 0) return GEMM_ERR_UNSUPPORTED;
+    if (resolved) *resolved = cfg;
+    return GEMM_OK;
+}
+
 int gemm_launch_plan(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* grid_ctas, int32_t* num_tiles,
                      int32_t* split_tiles)
 {
@@ -986,15 +1171,23 @@ int gemm_launch_plan(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t*
     if (rc != GEMM_OK) return rc;
     int64_t ctas = 0, split = 0;
     if (cfg == GEMM_TILE_256x256x64_PAIR || cfg == GEMM_TILE_256x256x128_PAIR ||
-        cfg == GEMM_TILE_256x256x128_PAIR_ALIGNED) {
+        cfg == GEMM_TILE_256x256x128_PAIR_ALIGNED || cfg == GEMM_TILE_256x256x64_PAIR_STREAMK) {
         int64_t clusters = 0;
-        rc = cfg == GEMM_TILE_256x256x64_PAIR    ? pair_clusters<CfgPair256>(d, cfg, &clusters)
-             : cfg == GEMM_TILE_256x256x128_PAIR ? pair_clusters<CfgPair256Deep>(d, cfg, &clusters)
-                                                 : pair_clusters<CfgPair256Aligned>(d, cfg, &clusters);
+        rc = cfg == GEMM_TILE_256x256x64_PAIR         ? pair_clusters<CfgPair256>(d, cfg, &clusters)
+             : cfg == GEMM_TILE_256x256x128_PAIR      ? pair_clusters<CfgPair256Deep>(d, cfg, &clusters)
+             : cfg == GEMM_TILE_256x256x128_PAIR_ALIGNED ? pair_clusters<CfgPair256Aligned>(d, cfg, &clusters)
+                                                      : pair_clusters<CfgPair256StreamK>(d, cfg, &clusters);
         if (rc != GEMM_OK) return rc;
-        split = split_tail_tiles(tiles, clusters);
-        const int64_t units = tiles + split;
-        ctas = 2 * (units < clusters ? units : clusters);
+        const int64_t sk = cfg == GEMM_TILE_256x256x64_PAIR_STREAMK ? streamk_tiles(tiles, (K + tk - 1) / tk, clusters)
+                                                                   : 0;
+        if (sk > 0) {  // stream-K: every resident cluster; split_tiles reports the stream-K tiles
+            split = sk;
+            ctas = 2 * clusters;
+        } else {
+            split = split_tail_tiles(tiles, clusters);
+            const int64_t units = tiles + split;
+            ctas = 2 * (units < clusters ? units : clusters);
+        }
     } else if (cfg == GEMM_TILE_128x128x64_SPLITK &&
                splitk_factor(tiles, (K + tk - 1) / tk, d->sm_count) > 1) {
         ctas = tiles * splitk_factor(tiles, (K + tk - 1) / tk, d->sm_count);  // one cluster per tile
@@ -1070,6 +1263,15 @@ int gemm_query_status(void* stream)
     if (word != 0) {
         e = cudaMemset(d->status, 0, sizeof(uint32_t));
         if (e != cudaSuccess) return cuda_fail(e);
+        // an aborted stream-K launch may have left flags raised: clear them once
+        // nothing of the device runs any more
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e);
+        rc = sk_clear_flags(dev);
+        if (rc != GEMM_OK) return rc;
     }
     return (word & kStatusTimeout) ? GEMM_ERR_TIMEOUT : GEMM_OK;
 }
@@ -1154,6 +1356,10 @@ int gemm_f16_f32acc_noalloc(const void* A, const void* B, void* C, int64_t M, in
     p.num_units = p.num_tiles;
     p.A = p.B = nullptr;
     p.lda = p.ldb = 0;
+    p.sk_first_tile = p.num_tiles;
+    p.sk_iters = 0;
+    p.sk_ws = nullptr;
+    p.sk_flags = nullptr;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The scratch keeps the previous call's contents: the status word starts at zero.

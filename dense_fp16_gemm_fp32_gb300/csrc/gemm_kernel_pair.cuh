@@ -29,6 +29,24 @@
 // clusters idle, the host marks those last pids as split; each is computed as
 // two 256 x 128 column halves (N = 128 MMAs) by two clusters, so the last wave
 // takes about half a tile's time. No partial sums cross CTAs.
+// Stream-K (PairCfg STREAMK): when the last partial wave holds more than half
+// of the clusters, the last wave plus one full wave of tiles are computed as
+// one contiguous range of (tile, k step) iterations per cluster: a cluster
+// first takes its whole tiles pid = cluster, cluster + clusters, ... below
+// sk_first_tile, then its iteration range, walked from its end: first the
+// head (the first k steps) of the tile its range ends in, last the tail of
+// the tile its range starts in (each range holds at least a tile's k steps,
+// so a tile is shared by at most two clusters, and the head of a shared
+// tile lies in the lower-numbered cluster). The head's fp32 partial sums go
+// to a workspace slot and a ready flag is raised; the tail, the cluster's
+// last unit, waits for the flag, copies the partial into its now idle stage
+// ring and adds it to its own sums before the one fp16 narrowing. A cluster
+// only ever waits on a lower-numbered one, which the hardware dispatched
+// before it and which raises the flag without waiting on anything. The sum
+// order is fixed by the launch: results are deterministic. This follows the stream-K decomposition (Osama, Merrill,
+// Cecka, Garland and Owens, "Stream-K: Work-centric Parallel Decomposition
+// for Dense Matrix-Matrix Multiplication on the GPU", PPoPP 2023), in its
+// hybrid form (whole tiles first, one stream-K wave and a half at the end).
 // Waits are bounded as in gemm_kernel.cuh. Before a CTA may exit, its
 // producer waits until every stage has been released (so no commit still
 // targets it) and the MMA thread waits until both epilogues have released
@@ -53,10 +71,14 @@ namespace gemm103 {
 // The host launches it only when M and N are multiples of 256 and K of TK;
 // the epilogue's edge tests are then compiled out (loads need none: a TMA box
 // never reaches past the tensor when the extents are whole tiles).
-template <int STAGES_, int TK_ = 64, bool ALIGNED_ = false>
+// STREAMK: the stream-K schedule described above (the host launches it only
+// when it applies; otherwise the plain form of the same configuration runs).
+template <int STAGES_, int TK_ = 64, bool ALIGNED_ = false, bool STREAMK_ = false>
 struct PairCfg {
     static constexpr int TM = 256, TN = 256, TK = TK_, STAGES = STAGES_;  // tile of the pair
     static constexpr bool ALIGNED = ALIGNED_;
+    static constexpr bool STREAMK = STREAMK_;
+    static_assert(!(ALIGNED && STREAMK), "one specialisation at a time");
     static_assert(TK == 64 || TK == 128, "stage depth of 64 or 128");
     static constexpr int CTA_M = 128;                                     // A / D rows per CTA
     static constexpr int CTA_N = 128;                                     // B columns per CTA
@@ -92,18 +114,32 @@ struct PairCfg {
     static constexpr int EPI_COLS_LAST = 64;
     static constexpr int WIDE_EPI_MAX_K = 1024;
     static constexpr int STAGING_BYTES = EPI_WARPS * EpiStaging<EPI_COLS_LAST>::WARP_BYTES;
-    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 8;
+    // stream-K: one partial-copy barrier per epilogue warp; each warp's partial
+    // (32 rows x 256 fp32) lands in its 32 KiB of the idle stage ring
+    static constexpr int SK_BARS = STREAMK ? EPI_WARPS : 0;
+    static constexpr uint32_t SK_WARP_BYTES = 32u * TN * 4u;
+    static_assert(!STREAMK || EPI_WARPS * SK_WARP_BYTES <= STAGES * (A_STAGE + B_STAGE), "partials fit the ring");
+    static constexpr int BAR_BYTES = (2 * STAGES + 5 + SK_BARS) * 8 + 8;
     static constexpr int SMEM_BYTES = 1024 + STAGES * (A_STAGE + B_STAGE) + STAGING_BYTES + BAR_BYTES;
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
     static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
 };
+
+// Role of a work unit's k range: the whole tile's, the head (first k steps)
+// of a stream-K tile shared with the next cluster (its partial goes to the
+// workspace), or the tail of one (which adds the head's partial before
+// narrowing).
+enum : int32_t { kUnitWhole = 0, kUnitHead = 1, kUnitTail = 2 };
 
 // Work unit u of the persistent schedule: the full tiles in pid order, then
 // the two column halves of each pid in [num_full_tiles, num_tiles), pid by pid.
 struct PairUnit {
     TileCoord tc;
     int32_t pid;
-    int32_t half;  // -1: the whole 256-column tile; 0 / 1: columns [0,128) / [128,256)
+    int32_t half;    // -1: the whole 256-column tile; 0 / 1: columns [0,128) / [128,256)
+    int32_t kb, ke;  // k steps [kb, ke) of the tile
+    int32_t role;    // kUnitWhole, kUnitHead or kUnitTail
+    bool last;       // the cluster's last unit
 };
 
 __device__ __forceinline__ PairUnit pair_unit(int32_t u, const GemmParams& p)
@@ -118,7 +154,89 @@ __device__ __forceinline__ PairUnit pair_unit(int32_t u, const GemmParams& p)
         r.half = v & 1;
     }
     r.tc = grouped_tile(r.pid, p.map);
+    r.kb = 0;
+    r.ke = p.num_k_tiles;
+    r.role = kUnitWhole;
     return r;
+}
+
+// The units one cluster processes, in order; every warp walks its own copy,
+// so the producer, MMA and epilogue warps see the same sequence.
+template <bool kStreamK>
+struct UnitWalk {
+    int32_t u, step;     // next whole-tile unit and the stride (the cluster count)
+    int32_t it, it_end;  // stream-K: the cluster's remaining iteration range, taken from its end
+
+    __device__ __forceinline__ UnitWalk(int32_t pair, int32_t num_pairs, const GemmParams& p)
+        : u(pair), step(num_pairs), it(0), it_end(0)
+    {
+        if constexpr (kStreamK) {
+            const int64_t T = p.sk_iters;
+            it = static_cast<int32_t>(static_cast<int64_t>(pair) * T / num_pairs);
+            it_end = static_cast<int32_t>(static_cast<int64_t>(pair + 1) * T / num_pairs);
+        }
+    }
+
+    __device__ __forceinline__ bool next(PairUnit& r, const GemmParams& p)
+    {
+        if constexpr (!kStreamK) {
+            if (u >= p.num_units) return false;
+            r = pair_unit(u, p);
+            u += step;
+            r.last = u >= p.num_units;
+            return true;
+        } else {
+            const int32_t KT = p.num_k_tiles;
+            if (u < p.sk_first_tile) {
+                r.pid = u;
+                r.kb = 0;
+                r.ke = KT;
+                r.role = kUnitWhole;
+                u += step;
+            } else {
+                if (it >= it_end) return false;
+                const int32_t t = (it_end - 1) / KT;
+                r.kb = max(it, t * KT) - t * KT;
+                r.ke = it_end - t * KT;
+                r.pid = p.sk_first_tile + t;
+                // a range holds at least KT iterations, so the piece where it
+                // ends begins at k step 0 (a head, unless the whole tile) and
+                // the piece where it starts runs to the last k step (a tail)
+                r.role = r.kb > 0 ? kUnitTail : (r.ke < KT ? kUnitHead : kUnitWhole);
+                it_end = t * KT + r.kb;
+            }
+            r.half = -1;
+            r.tc = grouped_tile(r.pid, p.map);
+            r.last = u >= p.sk_first_tile && it >= it_end;
+            return true;
+        }
+    }
+};
+
+// The stream-K workspace block of one epilogue warp: 32 rows x TN fp32, the
+// 16-byte chunk j (columns 4j .. 4j+3) of lane l's row at index j * 32 + l,
+// so that each store or load of a warp covers 512 contiguous bytes.
+template <int TN>
+__device__ __forceinline__ size_t sk_block(int32_t slot, uint32_t rank, int q)
+{
+    return ((static_cast<size_t>(slot) * 2 + rank) * 4 + static_cast<size_t>(q)) * (32u * TN);
+}
+
+// Stream-K tail: this warp's 32 accumulator rows, unrounded, to its workspace
+// block (see sk_block). release() runs once every tensor-memory read is done.
+template <int TN, class Release>
+__device__ __forceinline__ void epilogue_store_partial(uint32_t t_row, uint4* ws, int lane, Release release)
+{
+#pragma unroll 1
+    for (int c = 0; c < TN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+        tmem_ld_wait();
+        if (c == TN / 32 - 1) release();
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            ws[(c * 8 + j) * 32 + lane] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    }
 }
 
 template <class Cfg>
@@ -140,7 +258,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     uint64_t* acc_full = empty + Cfg::STAGES;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* drain = acc_empty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* sk_bar = drain + 1;  // Cfg::SK_BARS of them
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sk_bar + Cfg::SK_BARS);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -172,12 +291,15 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             mbar_init(&acc_empty[b], 2 * Cfg::EPI_WARPS);  // even CTA: every epilogue warp of the pair
         }
         mbar_init(drain, 1);
+        for (int b = 0; b < Cfg::SK_BARS; ++b) mbar_init(&sk_bar[b], 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
     cluster_arrive();
-    PairUnit first_un{};
-    if (warp == 0) first_un = pair_unit(pair, p);
+    UnitWalk<Cfg::STREAMK> walk(pair, num_pairs, p);  // the producer's walk: its first unit mapped here
+    PairUnit un0{};
+    bool have0 = false;
+    if (warp == 0) have0 = walk.next(un0, p);
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
         tmem_relinquish_alloc_permit_pair();
@@ -204,8 +326,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int32_t u = pair; ok && u < p.num_units; u += num_pairs) {
-                const PairUnit un = u == pair ? first_un : pair_unit(u, p);
+            PairUnit un = un0;
+            for (bool have = have0; ok && have; have = walk.next(un, p)) {
                 const int32_t m0 = un.tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M;
                 // whole tile: this CTA's 128 of 256 columns; half tile: its 64 of the half's 128
                 const int32_t n0 = un.half < 0 ? un.tc.pid_n * Cfg::TN + static_cast<int32_t>(rank) * Cfg::CTA_N
@@ -213,7 +335,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                                                      static_cast<int32_t>(rank) * (Cfg::CTA_N / 2);
                 const int nbox = un.half < 0 ? Cfg::CTA_N / 64 : Cfg::CTA_N / 128;
                 const uint32_t tx = un.half < 0 ? Cfg::PAIR_STAGE_TX : Cfg::PAIR_STAGE_TX_HALF;
-                for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
+                for (int32_t kt = un.kb; kt < un.ke; ++kt) {
                     ok = warp_wait_phase<true>(&empty[stage], phase ^ 1u, w, kWhereProducer);
                     if (!ok) break;
                     const uint32_t fb = full0_even + 8u * static_cast<uint32_t>(stage);
@@ -257,13 +379,14 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             bool ok = true;
             const uint32_t a_base = smem_addr(sA);
             const uint32_t b_base = smem_addr(sB);
-            for (int32_t u = pair; ok && u < p.num_units; u += num_pairs) {
-                const uint32_t idesc = u < p.num_full_tiles ? Cfg::IDESC : Cfg::IDESC_HALF;
+            PairUnit un;
+            while (ok && walk.next(un, p)) {
+                const uint32_t idesc = un.half < 0 ? Cfg::IDESC : Cfg::IDESC_HALF;
                 ok = warp_wait_phase<true>(&acc_empty[buf], acc_phase ^ 1u, w, kWhereMma);
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * Cfg::ACC_COLS;
-                for (int32_t kt = 0; kt < p.num_k_tiles; ++kt) {
+                for (int32_t kt = un.kb; kt < un.ke; ++kt) {
                     ok = warp_wait_phase(&full[stage], phase, w, kWhereMma);
                     if (!ok) break;
                     tc_fence_after_sync();
@@ -279,9 +402,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < Cfg::TK / 16; ++kk)
-                            tc_mma_f16_ss_pair(d_tmem, ad[kk], bd[kk], idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                            tc_mma_f16_ss_pair(d_tmem, ad[kk], bd[kk], idesc, (kt > un.kb || kk > 0) ? 1u : 0u);
                         tc_commit_pair_multicast(smem_addr(&empty[stage]), 0x3);  // the stage is free in both CTAs
-                        if (kt == p.num_k_tiles - 1)  // accumulator complete, in both CTAs
+                        if (kt == un.ke - 1)  // accumulator complete, in both CTAs
                             tc_commit_pair_multicast(smem_addr(&acc_full[buf]), 0x3);
                     }
                     __syncwarp();
@@ -318,10 +441,10 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
         const uint32_t acc_empty0_even = map_shared_to_rank(smem_addr(&acc_empty[0]), 0);
         int buf = 0;
         uint32_t acc_phase = 0;
-        for (int32_t u = pair; u < p.num_units; u += num_pairs) {
-            const PairUnit un = pair_unit(u, p);
+        PairUnit un;
+        while (walk.next(un, p)) {
             const TileCoord tc = un.tc;
-            if (p.trace != nullptr && un.half <= 0 && rank == 0 && warp == 2 && lane == 0) {
+            if (p.trace != nullptr && un.half <= 0 && un.role != kUnitHead && rank == 0 && warp == 2 && lane == 0) {
                 p.trace[3 * static_cast<int64_t>(un.pid) + 0] = tc.pid_m;
                 p.trace[3 * static_cast<int64_t>(un.pid) + 1] = tc.pid_n;
                 p.trace[3 * static_cast<int64_t>(un.pid) + 2] = pair;
@@ -353,7 +476,55 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const int32_t c_row0 = tc.pid_m * Cfg::TM + static_cast<int32_t>(rank) * Cfg::CTA_M + q * 32;
             uint8_t* staging = sC + (warp - 2) * EpiStaging<Cfg::EPI_COLS_LAST>::WARP_BYTES;
             constexpr bool kA = Cfg::ALIGNED;
-            if (u + num_pairs < p.num_units && p.K > Cfg::WIDE_EPI_MAX_K) {
+            if constexpr (Cfg::STREAMK) {
+                if (un.role != kUnitWhole) {
+                    const int32_t slot = un.pid - p.sk_first_tile;
+                    uint32_t* flag = p.sk_flags + (static_cast<size_t>(slot) * 2 + rank) * 4 + q;
+                    const float* blk = p.sk_ws + sk_block<Cfg::TN>(slot, rank, q);
+                    if (un.role == kUnitHead) {
+                        // the partial sums, then the flag (release at GPU scope, after every lane's stores)
+                        epilogue_store_partial<Cfg::TN>(t_row, reinterpret_cast<uint4*>(const_cast<float*>(blk)), lane,
+                                                        release);
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0) st_release_gpu(flag, 1u);
+                    } else {
+                        // tail, the cluster's last unit: its MMAs are complete, so the stage ring is
+                        // idle; the head's partial is copied into this warp's 32 KiB of it
+                        if (!warp_wait_flag(flag, w, kWhereEpilogue)) break;
+                        uint8_t* part = sA + static_cast<uint32_t>(q) * Cfg::SK_WARP_BYTES;
+                        if (lane == 0) {
+                            fence_proxy_async_global();
+                            mbar_arrive_expect_tx(&sk_bar[q], Cfg::SK_WARP_BYTES);
+                            bulk_load_1d(part, blk, Cfg::SK_WARP_BYTES, &sk_bar[q]);
+                        }
+                        if (!warp_wait_phase(&sk_bar[q], 0u, w, kWhereEpilogue)) break;
+                        const uint32_t part0 = smem_addr(part) + static_cast<uint32_t>(lane) * 16u;
+                        // tail sums + head sums, then the one narrowing
+                        const auto add = [&](int col, uint32_t(&r)[32]) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint4 v = ld_shared_v4(part0 + static_cast<uint32_t>((col / 4 + j) * 32 * 16));
+                                r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + __uint_as_float(v.x));
+                                r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + __uint_as_float(v.y));
+                                r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + __uint_as_float(v.z));
+                                r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + __uint_as_float(v.w));
+                            }
+                        };
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+                        epilogue_tma_store<Cfg::TN, Cfg::EPI_COLS_LAST>(t_row, staging, &tmap_c_last, c_row0, n0, p.M,
+                                                                        p.N, p.C, p.ldc, lane, release, add);
+                        if (lane == 0) *flag = 0u;  // consumed: the next launch starts from a cleared flag
+                    }
+                    if (++buf == 2) {
+                        buf = 0;
+                        acc_phase ^= 1u;
+                    }
+                    continue;
+                }
+            }
+            if (!un.last && p.K > Cfg::WIDE_EPI_MAX_K) {
                 if (un.half < 0)
                     epilogue_tma_store<Cfg::TN, Cfg::EPI_COLS, false, kA>(t_row, staging, &tmap_c, c_row0, n0, p.M,
                                                                           p.N, p.C, p.ldc, lane, release);

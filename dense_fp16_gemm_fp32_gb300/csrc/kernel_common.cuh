@@ -36,6 +36,15 @@ struct GemmParams {
     const uint16_t* A;
     const uint16_t* B;
     int64_t lda, ldb;
+    // Stream-K pair kernel only: pids [0, sk_first_tile) are whole tiles taken
+    // in turn by the clusters; the iterations (tile, k step) of pids
+    // [sk_first_tile, num_tiles), sk_iters in all, are split into one
+    // contiguous range per cluster. sk_ws holds one fp32 partial tile per
+    // stream-K pid, sk_flags one ready flag per pid, CTA and epilogue warp.
+    int32_t sk_first_tile;
+    int32_t sk_iters;
+    float* sk_ws;
+    uint32_t* sk_flags;
 };
 
 struct Watch {
@@ -97,6 +106,30 @@ __device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, 
     return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// Wait until the global flag is non-zero (acquire at GPU scope), every lane
+// polling. Bounded like wait_phase: false if the CTA is aborting or the wait
+// ran out (which starts the abort).
+__device__ __forceinline__ bool warp_wait_flag(const uint32_t* flag, const Watch& w, uint32_t where)
+{
+    bool ok = ld_acquire_gpu(flag) != 0u;
+    if (__all_sync(0xffffffffu, ok)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        ok = ld_acquire_gpu(flag) != 0u;
+        if (__all_sync(0xffffffffu, ok)) return true;
+        if (__any_sync(0xffffffffu, *w.abort != 0u)) return false;
+        if (__any_sync(0xffffffffu, global_timer_ns() - t0 > w.limit_ns)) {
+            if ((threadIdx.x & 31) == 0) {
+                *w.abort = 1u;
+                atomicOr(w.status, kStatusTimeout | (where << 8));
+            }
+            __syncwarp();
+            return false;
+        }
+        __nanosleep(100);
+    }
+}
+
 // C[row, n0 .. n0 + ncols) = +0 for the columns below N (the K == 0 case).
 // No element at or past column N is written.
 __device__ __forceinline__ void store_zero_row(uint16_t* crow, int32_t n0, int32_t ncols, int32_t N)
@@ -154,10 +187,17 @@ struct EpiStaging {
 // kAligned: the caller guarantees that the tile lies wholly inside C (M and N
 // whole multiples of the tile), so the edge tests are compiled out and every
 // block is one TMA store.
-template <int TN, int COLS, bool kDirect = false, bool kAligned = false, class Release>
+// add(col, r): called with the lane's fp32 accumulator bits of columns
+// [col, col + 32) of its row before they are narrowed (the stream-K finisher
+// adds the other k range's partial sums there); NoAddend does nothing.
+struct NoAddend {
+    __device__ __forceinline__ void operator()(int, uint32_t (&)[32]) const {}
+};
+
+template <int TN, int COLS, bool kDirect = false, bool kAligned = false, class Release, class Addend>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* staging, const CUtensorMap* tmap_c,
                                                    int32_t c_row0, int32_t n0, int32_t M, int32_t N,
-                                                   uint16_t* C, int64_t ldc, int lane, Release release)
+                                                   uint16_t* C, int64_t ldc, int lane, Release release, Addend add)
 {
     using St = EpiStaging<COLS>;
     static_assert(TN % COLS == 0, "whole blocks");
@@ -174,12 +214,14 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
                 uint32_t r1[32];
                 tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * COLS + 32), r1);
                 tmem_ld_wait();
+                add(c * COLS + 32, r1);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) h[16 + i] = pack_half2_rn(r1[2 * i], r1[2 * i + 1]);
             } else {
                 tmem_ld_wait();
             }
             if (c == TN / COLS - 1) release();
+            add(c * COLS, r0);
 #pragma unroll
             for (int i = 0; i < 16; ++i) h[i] = pack_half2_rn(r0[2 * i], r0[2 * i + 1]);
         }
@@ -229,6 +271,15 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
             bulk_commit_group();  // an empty group keeps the per-buffer accounting uniform
         }
     }
+}
+
+template <int TN, int COLS, bool kDirect = false, bool kAligned = false, class Release>
+__device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* staging, const CUtensorMap* tmap_c,
+                                                   int32_t c_row0, int32_t n0, int32_t M, int32_t N,
+                                                   uint16_t* C, int64_t ldc, int lane, Release release)
+{
+    epilogue_tma_store<TN, COLS, kDirect, kAligned>(t_row, staging, tmap_c, c_row0, n0, M, N, C, ldc, lane, release,
+                                                    NoAddend{});
 }
 
 // ---------------------------------------------------------------- generic loads

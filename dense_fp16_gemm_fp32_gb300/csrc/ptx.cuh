@@ -347,6 +347,47 @@ __device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t 
         : "memory");
 }
 
+// ---------------------------------------------------------------- global flags and bulk copies
+// 32-bit load with acquire semantics at GPU scope (pairs with st_release_gpu).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// 32-bit store with release semantics at GPU scope.
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses of global memory (and
+// what it acquired) before its later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Contiguous bulk copy global -> this CTA's shared memory, `bytes` (a multiple
+// of 16, both addresses 16-byte aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr)
+                 : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor of tcgen05.mma (64 bits):
 //   [0,14)  start address >> 4       [16,30) leading-dimension byte offset >> 4

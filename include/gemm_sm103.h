@@ -84,7 +84,9 @@ typedef enum {
                                  38 tiles of 256x256 (every one split into column halves),
                                  256x256x128_PAIR if K > 512, else 128x128x64; 128x256x64
                                  with fewer than 76 (less than one wave of CTA pairs) or
-                                 K <= 256; otherwise 256x256x64_PAIR up to K = 4096 and
+                                 K <= 256; 256x256x64_PAIR_STREAMK when K >= 4096, there are
+                                 at most 8 waves of 76 and the last one holds more than 38;
+                                 otherwise 256x256x64_PAIR up to K = 4096 and
                                  256x256x128_PAIR above */
     GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */
     GEMM_TILE_128x64x32 = 2,  /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
@@ -111,7 +113,22 @@ typedef enum {
                                  operands a tensor map cannot describe when no workspace is
                                  given. Never chosen by GEMM_TILE_AUTO (4 computes the same
                                  bits); gemm_autotune times it only on whole tiles */
-    GEMM_TILE_COUNT = 9       /* number of values above, GEMM_TILE_AUTO included */
+    GEMM_TILE_256x256x64_PAIR_STREAMK = 9, /* 3 with a stream-K schedule where the last partial
+                                 wave of tiles holds more than half of the resident clusters
+                                 (and there is at least one full wave): that wave and one full
+                                 wave are split by k iterations, one contiguous range per
+                                 cluster; a tile shared by two clusters has its first k steps'
+                                 fp32 partial sums passed through a workspace and added before
+                                 the one fp16 rounding (a fixed order: results are
+                                 deterministic). Elsewhere it runs as 3. The workspace (about
+                                 40 MB: 2 x resident clusters x 256 KiB, plus flags) is
+                                 allocated on the first stream-K launch on each stream of a
+                                 device and kept until exit; make that first call outside
+                                 stream capture (under capture without one, 3 runs instead).
+                                 Launches on one stream share it; do not replay a graph that
+                                 holds such a launch concurrently with other stream-K work of
+                                 the stream it was captured on */
+    GEMM_TILE_COUNT = 10      /* number of values above, GEMM_TILE_AUTO included */
 } gemm_tile_cfg_t;
 
 /*
@@ -250,6 +267,14 @@ int gemm_tile_shape(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* 
                     int32_t* tile_n, int32_t* tile_k);
 
 /*
+ * The tile configuration a tile_cfg (GEMM_TILE_AUTO included) resolves to
+ * for (M, N, K) on the current device: the configuration gemm_autotune chose
+ * for this shape, else the rule of GEMM_TILE_AUTO; other values map to
+ * themselves. GEMM_ERR_UNSUPPORTED for an unknown tile_cfg. No device work.
+ */
+int gemm_tile_config(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* resolved);
+
+/*
  * How the current device would schedule a problem (no kernel launch):
  *   grid_ctas    CTAs of the persistent grid (2 per cluster for the CTA-pair
  *                configurations)
@@ -260,7 +285,13 @@ int gemm_tile_shape(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* 
  *                ...: unit u < num_tiles - split_tiles is pid u; the remaining
  *                units are the halves of the last split_tiles pids, two per pid
  *                in pid order. A last wave of R tiles is split when 2R fits in
- *                one wave of clusters.
+ *                one wave of clusters. For GEMM_TILE_256x256x64_PAIR_STREAMK
+ *                when its stream-K schedule applies: the number S of
+ *                stream-K tiles (the last S pids); pids below num_tiles - S
+ *                are whole tiles taken in turn by the clusters, and the
+ *                S x ceil(K/64) iterations of the others are split into one
+ *                contiguous range per cluster, cluster c holding iterations
+ *                [c*I/C, (c+1)*I/C) (I iterations, C = grid_ctas / 2).
  * Host pointers, each may be NULL. Sets up the configuration's per-device
  * state on first use (like a launch). GEMM_ERR_CUDA without a device.
  */
@@ -297,7 +328,10 @@ int gemm_tile_map_host(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n, int
  * Synchronises `stream`, then reads and clears the current device's status
  * word. Returns GEMM_ERR_TIMEOUT if a kernel launched since the last query
  * gave up on a bounded wait (its output is then incomplete), GEMM_OK
- * otherwise, or GEMM_ERR_CUDA if synchronisation failed.
+ * otherwise, or GEMM_ERR_CUDA if synchronisation failed. After a timeout it
+ * also synchronises the device and clears the ready flags of the device's
+ * stream-K workspaces (an aborted launch may leave one raised); query the
+ * status after a timeout before launching more stream-K work.
  */
 int gemm_query_status(void* stream);
 

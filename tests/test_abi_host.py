@@ -58,6 +58,15 @@ def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=4096) == (128, 128, 64)    # split-K
     assert g.tile_shape(g.TILE_AUTO, M=8192, N=8192, K=8192) == (256, 256, 128)
     assert g.tile_shape(g.TILE_AUTO, M=16384, N=16384, K=16384) == (256, 256, 128)
+    # stream-K: 192 pair tiles (a last wave of 40 of 76) with K >= 4096; not for shorter K or many waves
+    assert g.tile_config(g.TILE_AUTO, M=4096, N=3072, K=8192) == g.TILE_256x256x64_PAIR_STREAMK
+    assert g.tile_config(g.TILE_AUTO, M=4096, N=3072, K=4096) == g.TILE_256x256x64_PAIR_STREAMK
+    assert g.tile_config(g.TILE_AUTO, M=4096, N=3072, K=2048) == g.TILE_256x256x64_PAIR
+    assert g.tile_config(g.TILE_AUTO, M=4095, N=3000, K=1000) == g.TILE_256x256x64_PAIR
+    assert g.tile_config(g.TILE_AUTO, M=8192, N=8192, K=8192) == g.TILE_256x256x128_PAIR   # last wave of 36
+    assert g.tile_config(g.TILE_AUTO, M=16384, N=16384, K=16384) == g.TILE_256x256x128_PAIR  # 54 waves
+    assert g.tile_config(g.TILE_256x256x128_PAIR_ALIGNED, 8, 8, 8) == g.TILE_256x256x128_PAIR_ALIGNED
+    assert g.tile_shape(g.TILE_256x256x64_PAIR_STREAMK) == (256, 256, 64)
     assert g.tile_shape(g.TILE_256x256x64_PAIR) == (256, 256, 64)
     assert g.tile_shape(g.TILE_256x256x128_PAIR) == (256, 256, 128)
     assert g.tile_shape(g.TILE_128x256x64) == (128, 256, 64)

@@ -35,6 +35,7 @@ def capture(fn):
     (512, 512, 512, g.TILE_128x128x64_SPLITK),         # cluster split-K
     (1024, 768, 128, g.TILE_AUTO),                     # 128 x 64 x 64 tiles
     (1000, 37, 1000, g.TILE_AUTO),                     # N not a multiple of 8: the workspace route
+    (4095, 3000, 1000, g.TILE_256x256x64_PAIR_STREAMK),  # stream-K: the capture stream's workspace
 ])
 def test_gemm_graph_replay_matches_eager(gemm_lib, M, N, K, cfg):
     A, B = inputs.gemm_inputs(M, N, K, seed=M + N + K)
