@@ -22,6 +22,10 @@ the host and copied to the device before timing). Rank 0 prints one JSON line.
   clock samples taken under load inside it, TFLOP/s per GHz and the fraction
   of the measured sustained bf16 rate. The timed steps of `value` are a burst
   when they last less than the power cap's settling time.
+  Workloads below the ridge (fewer flops per compulsory byte than the
+  measured tensor rate over the measured HBM bandwidth: the 512^3 check and
+  the worked example) are judged against HBM instead: compulsory bytes
+  2(MK + KN + MN) per launch over the launch time, the tensor figures beside.
 * pct_of_peak: the kernel's rate against NVIDIA's published dense fp16/bf16
   tensor-core rate of one GB300 (2.25 PFLOP/s: 36 PFLOP/s per 8 GPUs with
   2:4 sparsity, halved); roofline.frac is against the measured rate.
@@ -338,8 +342,12 @@ def run_ours(args, w, rank, world, local_rank):
     a, b = A.to(dev), B.to(dev)
     c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
     tm, tn, tk = g.tile_shape(args.tile_cfg, w.M, w.N, w.K)
+    resolved = g.tile_config(args.tile_cfg, w.M, w.N, w.K)
     tile = f"{tm}x{tn}x{tk}" + ("_pair" if tm == 256 else "")  # e.g. 256x256x128_pair
-    kernel_name = "gemm_f16_f32acc_pair_kernel" if tm == 256 else "gemm_f16_f32acc_kernel"
+    tile += {g.TILE_256x256x64_PAIR_STREAMK: "_streamk", g.TILE_256x256x128_PAIR_ALIGNED: "_aligned",
+             g.TILE_128x128x64_SPLITK: "_splitk"}.get(resolved, "")
+    kernel_name = ("gemm_f16_f32acc_pair_kernel" if tm == 256 else
+                   "gemm_f16_f32acc_splitk_kernel" if resolved == g.TILE_128x128x64_SPLITK else "gemm_f16_f32acc_kernel")
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
 
@@ -439,6 +447,31 @@ def run_ours(args, w, rank, world, local_rank):
                     "pct_of_nominal_peak": 100.0 * sus_tflops / NOMINAL_F16_TFLOPS,
                     "clocks": sus_clocks}
     main_s = (t_host1 - t_host0)
+    # Below the ridge (peak flops / HBM bytes per second) the kernel is judged
+    # against HBM: compulsory bytes 2(MK + KN + MN) per launch over its time.
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    compulsory = 2.0 * (w.M * w.K + w.K * w.N + w.M * w.N)
+    ridge = peak * 1e12 / (hbm * 1e9)
+    tensor_roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                   "traffic": load_traffic(f"{w.name}/{tile}/G{args.group_size_m}"),
+                   "peak_source": f"{peak_src} dense bf16 rate of cuBLAS in a burst (bf16_tflops, "
+                                  "MEASURED_PEAKS.json), the reference for a kernel timed alone; fp16 and bf16 "
+                                  "share the tensor rate"}
+    hbm_achieved = compulsory / (kernel_ms * 1e-3) / 1e9
+    hbm_roof = {"bound": "hbm", "achieved": hbm_achieved, "peak": hbm, "unit": "GB/s", "frac": hbm_achieved / hbm,
+                "traffic": tensor_roof["traffic"],
+                "peak_source": f"{peak_src} HBM copy bandwidth (hbm_gbs, MEASURED_PEAKS.json)",
+                "bytes_per_launch": compulsory}
+    below_ridge = flops / compulsory < ridge
+    roof = dict(hbm_roof if below_ridge else tensor_roof)
+    roof.update({"intensity_flop_per_byte": flops / compulsory, "ridge_flop_per_byte": ridge,
+                 "timed_region_s": main_s,
+                 "regime": ("burst: the timed steps last less than the power cap's settling time; "
+                            "the sustained key holds the power-capped rate")
+                           if main_s < 1.0 else "seconds-long timed region",
+                 "kernel": f"{kernel_name} {tile}", "kernel_ms": kernel_ms, "flops_per_launch": flops})
+    if below_ridge:
+        roof["tensor"] = {k: tensor_roof[k] for k in ("achieved", "peak", "unit", "frac")}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
@@ -446,17 +479,7 @@ def run_ours(args, w, rank, world, local_rank):
         "config": config_dict(w, args, tile),
         "pct_of_peak": 100.0 * achieved / NOMINAL_F16_TFLOPS,
         "nominal_peak": {"value": NOMINAL_F16_TFLOPS, "unit": UNIT, "source": NOMINAL_F16_SOURCE},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": load_traffic(f"{w.name}/{tile}/G{args.group_size_m}"),
-                     "peak_source": f"{peak_src} dense bf16 rate of cuBLAS in a burst (bf16_tflops, "
-                                    "MEASURED_PEAKS.json), the reference for a kernel timed alone; fp16 and bf16 "
-                                    "share the tensor rate",
-                     "timed_region_s": main_s,
-                     "regime": ("burst: the timed steps last less than the power cap's settling time; "
-                                "the sustained key holds the power-capped rate")
-                               if main_s < 1.0 else "seconds-long timed region",
-                     "kernel": f"{kernel_name} {tile}", "kernel_ms": kernel_ms,
-                     "flops_per_launch": flops},
+        "roofline": roof,
         "sustained": sus_line,
         "e2e": {"value": whole_job_tflops(flops, e2e_steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": 2 * (w.M * w.K + w.K * w.N), "d2h_bytes_per_step": 2 * w.M * w.N,
