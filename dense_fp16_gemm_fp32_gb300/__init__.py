@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     SOFTMAX_MAX_COLS,
     TILE_128x64x32,
     TILE_128x64x64,
+    TILE_64x64x64,
     TILE_128x128x64,
     TILE_128x128x64_SPLITK,
     TILE_128x256x64,

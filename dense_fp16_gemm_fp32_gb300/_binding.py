@@ -31,7 +31,8 @@ TILE_128x128x64_SPLITK = 6
 TILE_128x64x64 = 7
 TILE_256x256x128_PAIR_ALIGNED = 8
 TILE_256x256x64_PAIR_STREAMK = 9
-TILE_COUNT = 10
+TILE_64x64x64 = 10
+TILE_COUNT = 11
 
 DEFAULT_GROUP_SIZE_M = 8
 

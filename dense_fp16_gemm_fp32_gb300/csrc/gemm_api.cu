@@ -25,6 +25,7 @@ using Cfg128x64 = TileCfg<128, 64, 32, 6>;
 using Cfg128x128 = TileCfg<128, 128, 64, 6>;
 using CfgSplitK = TileCfg<128, 128, 64, 4>;  // the ring also holds the 64 KiB fp32 partial tile
 using Cfg128x64x64 = TileCfg<128, 64, 64, 8>;
+using Cfg64x64x64 = TileCfg<64, 64, 64, 8>;
 using CfgGeneric = TileCfg<128, 256, 64, 4, true>;  // plain loads and stores (operands TMA cannot address)
 constexpr int kGenericCfgId = 15;  // per-device launch state slot of the generic-load kernel
 constexpr int kMaxSplitK = 8;  // portable cluster size
@@ -264,6 +265,11 @@ int32_t tuned_cfg(int64_t M, int64_t N, int64_t K)
 //    for the one-CTA 128 x 256 tile; 512x512x2048 6.7 against 8.1 for the pair
 //    tile; 128x4096x1536 6.4 against 8.2 for 128 x 64 x 64; with two or more
 //    bands at K = 1024 the pair tile is 4-7 % faster);
+//  * 64 x 64 tiles that fit one wave (kOneWave), with M <= 128 or K <=
+//    kSmallK: the one-CTA 64 x 64 x 64 tile (tcgen05 M = 64), twice the SMs
+//    of 128 x 64 (512^3 3.81 us against 4.14; 768x768x512 3.90 against 4.20;
+//    256x2048x512 3.87 against 4.19; past one wave it loses: 1024x768x128
+//    2.96 against 2.69, 1024x1024x512 5.80 against 4.29);
 //  * 128 x 64 tiles that fit one wave (kOneWave) with at most one 128-row band
 //    or K <= kSmallK: the one-CTA 128 x 64 x 64 tile (512^3 4.14 us against
 //    4.50 for the pair tile and 4.78 for 128 x 128; 1024x768x128 2.70 against
@@ -308,8 +314,10 @@ int auto_cfg(int64_t M, int64_t N, int64_t K)
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     const int64_t small_tiles = ((M + 127) / 128) * ((N + 127) / 128);
     const int64_t narrow_tiles = ((M + 127) / 128) * ((N + 63) / 64);
+    const int64_t m64_tiles = ((M + 63) / 64) * ((N + 63) / 64);
     if (small_tiles <= kSplitKMaxTiles && (K >= kSplitKMinK || (M <= 128 && K >= kSplitKNarrowMinK)))
         return GEMM_TILE_128x128x64_SPLITK;
+    if (m64_tiles <= kOneWave && (M <= 128 || K <= kSmallK)) return GEMM_TILE_64x64x64;
     if (narrow_tiles <= kOneWave && (M <= 128 || K <= kSmallK)) return GEMM_TILE_128x64x64;
     if (M <= 128) return GEMM_TILE_128x256x64;
     if (2 * pair_tiles <= kOnePairWave) return K > kSmallK ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x128x64;
@@ -354,6 +362,9 @@ int resolve_cfg(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t* tm, 
         case GEMM_TILE_256x256x64_PAIR_STREAMK:
             *tm = CfgPair256StreamK::TM, *tn = CfgPair256StreamK::TN, *tk = CfgPair256StreamK::TK;
             return GEMM_TILE_256x256x64_PAIR_STREAMK;
+        case GEMM_TILE_64x64x64:
+            *tm = Cfg64x64x64::TM, *tn = Cfg64x64x64::TN, *tk = Cfg64x64x64::TK;
+            return GEMM_TILE_64x64x64;
         default:
             return -1;
     }
@@ -413,9 +424,9 @@ int launch(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stream)
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
     std::memset(&mc, 0, sizeof(mc));
-    // C: EPI_COLS x 32-row store boxes with the epilogue staging's swizzle
+    // C: EPI_COLS x EPI_ROWS store boxes with the epilogue staging's swizzle
     if (!Cfg::kGeneric)
-        rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, Cfg::EPI_COLS, 32,
+        rc = make_map(&mc, pr.C, pr.N, pr.M, pr.ldc, Cfg::EPI_COLS, Cfg::EPI_ROWS,
                       Cfg::EPI_COLS == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc != GEMM_OK) return rc;
     if (pr.K > 0 && !Cfg::kGeneric) {
@@ -969,6 +980,8 @@ int dispatch_tma(const Problem& pr, int cfg, int32_t* trace, cudaStream_t s)
             return launch_pair<CfgPair256Aligned>(pr, cfg, trace, s);
         case GEMM_TILE_256x256x64_PAIR_STREAMK:
             return launch_streamk(pr, trace, s);
+        case GEMM_TILE_64x64x64:
+            return launch<Cfg64x64x64>(pr, cfg, trace, s);
         default:
             return launch<Cfg128x256>(pr, cfg, trace, s);
     }

@@ -54,7 +54,10 @@ template <int TM_, int TN_, int TK_, int STAGES_, bool kGeneric_ = false>
 struct TileCfg {
     static constexpr int TM = TM_, TN = TN_, TK = TK_, STAGES = STAGES_;
     static constexpr bool kGeneric = kGeneric_;
-    static_assert(TM == 128, "one-CTA tcgen05 tile: 128 accumulator lanes");
+    // M = 128: row i of the accumulator in tensor-memory lane i. M = 64: rows
+    // 16q .. 16q + 15 in the first 16 lanes of lane quadrant q (each epilogue
+    // warp reads its quadrant and keeps 16 rows).
+    static_assert(TM == 128 || TM == 64, "one-CTA tcgen05 tile of 128 or 64 rows");
     static_assert(TN % 64 == 0 && TN >= 64 && TN <= 256, "B is loaded in 64-column boxes; MMA N <= 256");
     static_assert(TK == 64 || TK == 32, "A rows of 128 B (128B swizzle) or 64 B (64B swizzle)");
     static_assert(!kGeneric || TK == 64, "generic loads write the 128-byte swizzle");
@@ -83,6 +86,7 @@ struct TileCfg {
                                         : (2 * TN <= 256) ? 256 : 512;
 
     static constexpr int EPI_WARPS = EPI_THREADS / 32;
+    static constexpr int EPI_ROWS = TM / EPI_WARPS;  // accumulator rows per epilogue warp
     static constexpr int EPI_COLS = TN >= 64 ? 64 : 32;  // columns per epilogue store block
     static constexpr int STAGING_BYTES = EPI_WARPS * EpiStaging<EPI_COLS>::WARP_BYTES;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 8;
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
-        const int row = q * 32 + lane;
+        const int row = q * Cfg::EPI_ROWS + lane;  // valid for lane < EPI_ROWS
         int buf = 0;
         uint32_t acc_phase = 0;
         for (int32_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             const int32_t n0 = tc.pid_n * Cfg::TN;
             uint16_t* crow = p.C + static_cast<int64_t>(gm) * p.ldc;
             if (p.num_k_tiles == 0) {  // K == 0: the empty sum
-                if (gm < p.M) store_zero_row(crow, n0, Cfg::TN, p.N);
+                if (lane < Cfg::EPI_ROWS && gm < p.M) store_zero_row(crow, n0, Cfg::TN, p.N);
                 continue;
             }
             bool ok = wait_phase(&acc_full[buf], acc_phase, w, kWhereEpilogue);
@@ -309,8 +313,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::TN);
             uint64_t* release_bar = &acc_empty[buf];
-            epilogue_tma_store<Cfg::TN, Cfg::EPI_COLS, Cfg::kGeneric>(t_row, sC + (warp - 2) * EpiStaging<Cfg::EPI_COLS>::WARP_BYTES, &tmap_c,
-                                        tc.pid_m * Cfg::TM + q * 32, n0, p.M, p.N, p.C, p.ldc, lane, [&]() {
+            epilogue_tma_store<Cfg::TN, Cfg::EPI_COLS, Cfg::kGeneric, false, Cfg::EPI_ROWS>(t_row, sC + (warp - 2) * EpiStaging<Cfg::EPI_COLS>::WARP_BYTES, &tmap_c,
+                                        tc.pid_m * Cfg::TM + q * Cfg::EPI_ROWS, n0, p.M, p.N, p.C, p.ldc, lane, [&]() {
                                             tc_fence_before_sync();
                                             __syncwarp();
                                             if (lane == 0) mbar_arrive(release_bar);

@@ -194,11 +194,16 @@ struct NoAddend {
     __device__ __forceinline__ void operator()(int, uint32_t (&)[32]) const {}
 };
 
-template <int TN, int COLS, bool kDirect = false, bool kAligned = false, class Release, class Addend>
+// ROWS: accumulator rows per warp, 32 (M = 128 tiles) or 16 (M = 64 tiles,
+// whose rows sit in the first 16 lanes of each warp's 32: the other lanes'
+// values are read and dropped; C's tensor map then has 16-row boxes).
+template <int TN, int COLS, bool kDirect = false, bool kAligned = false, int ROWS = 32, class Release, class Addend>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* staging, const CUtensorMap* tmap_c,
                                                    int32_t c_row0, int32_t n0, int32_t M, int32_t N,
                                                    uint16_t* C, int64_t ldc, int lane, Release release, Addend add)
 {
+    static_assert(ROWS == 32 || ROWS == 16, "32 or 16 rows per warp");
+    const bool live = lane < ROWS;
     using St = EpiStaging<COLS>;
     static_assert(TN % COLS == 0, "whole blocks");
     const uint32_t stage0 = smem_addr(staging);
@@ -229,7 +234,7 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
         static_assert(!(kDirect && kAligned), "the aligned form stores through TMA");
         if (kDirect || (!kAligned && (N & 7) != 0 && x + COLS > N)) {  // or right edge inside a 16-byte granule
             const int32_t row = c_row0 + lane;
-            if (row < M && x < N) {
+            if (live && row < M && x < N) {
                 uint16_t* dst = C + static_cast<int64_t>(row) * ldc + x;
                 if (x + COLS <= N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
 #pragma unroll
@@ -260,10 +265,12 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
                 bulk_wait_group_read<1>();
         }
         __syncwarp();
+        if (live) {
 #pragma unroll
-        for (int j = 0; j < St::CHUNKS; ++j)
-            st_shared_v4(buf + row_off + ((static_cast<uint32_t>(j) ^ swz) << 4), h[4 * j], h[4 * j + 1], h[4 * j + 2],
-                         h[4 * j + 3]);
+            for (int j = 0; j < St::CHUNKS; ++j)
+                st_shared_v4(buf + row_off + ((static_cast<uint32_t>(j) ^ swz) << 4), h[4 * j], h[4 * j + 1],
+                             h[4 * j + 2], h[4 * j + 3]);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -273,13 +280,13 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* stag
     }
 }
 
-template <int TN, int COLS, bool kDirect = false, bool kAligned = false, class Release>
+template <int TN, int COLS, bool kDirect = false, bool kAligned = false, int ROWS = 32, class Release>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t t_row, uint8_t* staging, const CUtensorMap* tmap_c,
                                                    int32_t c_row0, int32_t n0, int32_t M, int32_t N,
                                                    uint16_t* C, int64_t ldc, int lane, Release release)
 {
-    epilogue_tma_store<TN, COLS, kDirect, kAligned>(t_row, staging, tmap_c, c_row0, n0, M, N, C, ldc, lane, release,
-                                                    NoAddend{});
+    epilogue_tma_store<TN, COLS, kDirect, kAligned, ROWS>(t_row, staging, tmap_c, c_row0, n0, M, N, C, ldc, lane,
+                                                          release, NoAddend{});
 }
 
 // ---------------------------------------------------------------- generic loads

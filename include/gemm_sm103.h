@@ -79,8 +79,8 @@ typedef enum {
                                  this (M, N, K) on the current device; else 128x128x64_SPLITK
                                  when there are at most 38 tiles of 128x128 and K >= 2048
                                  (K >= 1024 when M <= 128);
-                                 128x64x64 when its tiles fit one wave (at most 152) and
-                                 M <= 128 or K <= 512; 128x256x64 when M <= 128; with at most
+                                 64x64x64 when its tiles fit one wave (at most 152) and
+                                 M <= 128 or K <= 512; else 128x64x64 on the same terms; 128x256x64 when M <= 128; with at most
                                  38 tiles of 256x256 (every one split into column halves),
                                  256x256x128_PAIR if K > 512, else 128x128x64; 128x256x64
                                  with fewer than 76 (less than one wave of CTA pairs) or
@@ -128,7 +128,10 @@ typedef enum {
                                  Launches on one stream share it; do not replay a graph that
                                  holds such a launch concurrently with other stream-K work of
                                  the stream it was captured on */
-    GEMM_TILE_COUNT = 10      /* number of values above, GEMM_TILE_AUTO included */
+    GEMM_TILE_64x64x64 = 10,  /* 1 CTA per 64x64 tile (tcgen05 M = 64), 8 stages: twice the
+                                 CTAs of 128x64x64 for problems whose time is each SM's
+                                 operand loads */
+    GEMM_TILE_COUNT = 11      /* number of values above, GEMM_TILE_AUTO included */
 } gemm_tile_cfg_t;
 
 /*

@@ -39,7 +39,8 @@ def test_status_strings(lib):
 
 
 def test_tile_shapes(lib):
-    assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=512) == (128, 64, 64)      # one band, 64 tiles of 128x64
+    assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=512) == (64, 64, 64)       # one band, 128 tiles of 64x64
+    assert g.tile_shape(g.TILE_AUTO, M=128, N=8192, K=512) == (128, 64, 64)      # 256 tiles of 64x64: 128x64
     assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=1024) == (128, 128, 64)    # one band, 32 tiles: split-K
     assert g.tile_shape(g.TILE_AUTO, M=256, N=2048, K=1024) == (256, 256, 128)   # two bands at K = 1024: pair
     assert g.tile_shape(g.TILE_AUTO, M=128, N=16384, K=1024) == (128, 256, 64)   # one band, 256 tiles of 128x64
@@ -50,7 +51,7 @@ def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4096) == (256, 256, 64)   # 80 pair tiles, K <= 4096
     assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4097) == (256, 256, 128)  # deeper K
     assert g.tile_shape(g.TILE_AUTO, M=4096, N=3072, K=256) == (128, 256, 64)    # few k steps
-    assert g.tile_shape(g.TILE_AUTO, M=512, N=512, K=512) == (128, 64, 64)       # 32 tiles of 128x64, short K
+    assert g.tile_shape(g.TILE_AUTO, M=512, N=512, K=512) == (64, 64, 64)        # 64 tiles of 64x64, short K
     assert g.tile_shape(g.TILE_AUTO, M=1024, N=1024, K=512) == (128, 64, 64)     # 128 of them: one wave
     assert g.tile_shape(g.TILE_AUTO, M=1024, N=1024, K=1024) == (256, 256, 128)  # few, long enough K
     assert g.tile_shape(g.TILE_AUTO, M=1024, N=768, K=128) == (128, 64, 64)

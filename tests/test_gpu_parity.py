@@ -17,7 +17,7 @@ from _gpu_util import check_against_oracle
 pytestmark = pytest.mark.gpu
 
 ALL_CFGS = [g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR,
-            g.TILE_128x128x64, g.TILE_128x128x64_SPLITK, g.TILE_128x64x64]
+            g.TILE_128x128x64, g.TILE_128x128x64_SPLITK, g.TILE_128x64x64, g.TILE_64x64x64]
 
 
 @pytest.mark.parametrize("w", inputs.WORKLOADS, ids=lambda w: w.name)
@@ -34,7 +34,8 @@ def test_workload_parity(gemm_lib, w):
 
 @pytest.mark.parametrize("w", [w for w in inputs.WORKLOADS if w.tile_cfg == 0], ids=lambda w: w.name)
 @pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR,
-                                 g.TILE_128x128x64, g.TILE_128x128x64_SPLITK, g.TILE_128x64x64])
+                                 g.TILE_128x128x64, g.TILE_128x128x64_SPLITK, g.TILE_128x64x64,
+                                 g.TILE_64x64x64])
 def test_workload_parity_each_large_tile(gemm_lib, w, cfg):
     A, B = inputs.gemm_inputs(w.M, w.N, w.K, w.seed)
     C = g.gemm(A.cuda(), B.cuda(), group_size_m=w.group_size_m, tile_cfg=cfg)

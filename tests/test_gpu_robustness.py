@@ -22,7 +22,7 @@ CANARY = 0x7E01  # a quiet-NaN fp16 bit pattern the kernel never produces from f
 
 
 @pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR,
-                                 g.TILE_128x128x64, g.TILE_128x128x64_SPLITK, g.TILE_128x64x64, "generic"])
+                                 g.TILE_128x128x64, g.TILE_128x128x64_SPLITK, g.TILE_128x64x64, g.TILE_64x64x64, "generic"])
 def test_watchdog_timeout_reports_and_recovers(gemm_lib, cfg):
     A, B = inputs.gemm_inputs(256, 512, 128, seed=41)
     a, b = A.cuda(), B.cuda()
@@ -46,7 +46,7 @@ def test_watchdog_timeout_reports_and_recovers(gemm_lib, cfg):
 
 
 @pytest.mark.parametrize("cfg", [g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR,
-                                 g.TILE_128x128x64, g.TILE_128x128x64_SPLITK, g.TILE_128x64x64])
+                                 g.TILE_128x128x64, g.TILE_128x128x64_SPLITK, g.TILE_128x64x64, g.TILE_64x64x64])
 @pytest.mark.parametrize("M,N,K", [(129, 264, 72), (4095, 3000, 1000), (1, 8, 8), (300, 8, 1000), (300, 999, 1001)])
 def test_no_store_outside_c(gemm_lib, M, N, K, cfg):
     A, B = inputs.gemm_inputs(M, N, K, seed=M + N + K)

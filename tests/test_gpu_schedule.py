@@ -69,6 +69,8 @@ def _kernel_trace(M, N, K, G, cfg, seed):
     (1024, 768, 128, 2, g.TILE_128x64x64),     # the worked example's 96 tiles, 64-deep k steps
     (4095, 3000, 200, 3, g.TILE_128x64x64),    # 32 x 47 tiles: several per CTA
     (4095, 3000, 200, 3, g.TILE_128x64x32),    # the same with 32-deep k steps
+    (512, 512, 512, 8, g.TILE_64x64x64),       # 64 tiles of 64 rows (tcgen05 M = 64)
+    (4095, 3000, 200, 5, g.TILE_64x64x64),     # 64 x 47 tiles: several per CTA, clamped band
 ])
 def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
     A, B, C, tr, TM, TN = _kernel_trace(M, N, K, G, cfg, seed=31)

@@ -23,7 +23,7 @@ from _gpu_util import tolerance
 pytestmark = pytest.mark.gpu
 
 CFGS = [g.TILE_AUTO, g.TILE_128x256x64, g.TILE_128x64x32, g.TILE_256x256x128_PAIR, g.TILE_128x128x64,
-        g.TILE_128x128x64_SPLITK, g.TILE_128x64x64, "generic"]
+        g.TILE_128x128x64_SPLITK, g.TILE_128x64x64, g.TILE_64x64x64, "generic"]
 
 
 def run(A: torch.Tensor, B: torch.Tensor, cfg) -> np.ndarray:
