@@ -75,13 +75,32 @@ def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_128x128x64) == (128, 128, 64)
     assert g.tile_shape(g.TILE_128x128x64_SPLITK) == (128, 128, 64)
     assert g.tile_shape(g.TILE_128x64x64) == (128, 64, 64)
-    with pytest.raises(g.GemmError) as e:
-        g.tile_shape(17)
-    assert e.value.code == g.GEMM_ERR_UNSUPPORTED
+    assert g.tile_shape(g.TILE_64x64x64) == (64, 64, 64)
+    assert g.tile_shape(g.TILE_256x256x128_PAIR_ALIGNED) == (256, 256, 128)
+    assert g.TILE_COUNT == 11
+    for bad in (17, g.TILE_COUNT, -1):
+        with pytest.raises(g.GemmError) as e:
+            g.tile_shape(bad)
+        assert e.value.code == g.GEMM_ERR_UNSUPPORTED
+        with pytest.raises(g.GemmError) as e:
+            g.tile_config(bad, 64, 64, 64)
+        assert e.value.code == g.GEMM_ERR_UNSUPPORTED
+    # every named configuration resolves to itself; AUTO to one of them
+    for cfg in range(1, g.TILE_COUNT):
+        assert g.tile_config(cfg, 4095, 3000, 1000) == cfg
+    assert 1 <= g.tile_config(g.TILE_AUTO, 4095, 3000, 1000) < g.TILE_COUNT
 
 
 def _call(lib, A=16, B=16, C=16, M=64, N=64, K=64, G=8, cfg=0):
     return lib.gemm_f16_f32acc_tiled(A, B, C, M, N, K, G, cfg, None, None)
+
+
+def test_aligned_configuration_refuses_partial_tiles_before_any_cuda_call(lib):
+    # validation and the whole-tile promise are checked on the host, before a device is touched
+    big = 1 << 40
+    aligned = g.TILE_256x256x128_PAIR_ALIGNED
+    for (M, N, K) in ((255, 256, 128), (256, 264, 128), (256, 256, 136), (4095, 3000, 1000)):
+        assert _call(lib, big, 2 * big, 3 * big, M, N, K, cfg=aligned) == g.GEMM_ERR_UNSUPPORTED
 
 
 def test_validation_without_gpu(lib):
