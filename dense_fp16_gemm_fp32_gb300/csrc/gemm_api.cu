@@ -281,10 +281,12 @@ int32_t tuned_cfg(int64_t M, int64_t N, int64_t K)
 //    128-deep tile when K > kSmallK (2048x1024x1024 6.49 us against 8.34 for
 //    128 x 256; 768^3 4.96 against 5.22 for 128 x 64 x 64), else the one-CTA
 //    128 x 128 tile (2048x1024x512 4.96 against 5.05 for the pair tile);
-//  * less than one wave of pair tiles, or K <= kShortK: the one-CTA
-//    128 x 256 tile, whose epilogue and operand loads suit few k steps
-//    (4096x3072x128 7.25 us; with 40 to 64 pair tiles all of 128 x 256 and
-//    the two pair depths lie within 3 %);
+//  * less than one wave of pair tiles with K < kPairMinK, or K <= kShortK:
+//    the one-CTA 128 x 256 tile, whose epilogue and operand loads suit few k
+//    steps (4096x3072x128 7.25 us; 2048x2048x1024 8.67 against 8.80 for the
+//    64-deep pair tile); from K = kPairMinK the pair tile is 3-6 % faster
+//    there (2048^3 13.46 against 13.84 us, 2048x2048x4096 21.98 against
+//    23.41, 2048x1536x3072 and its 48 tiles 17.48 against 18.60);
 //  * otherwise the CTA-pair tile: 64-deep stages (six) up to K = kDeepK
 //    (4096^3 75.7 us against 77.2, ragged 4095x3000x1000 25.9 against 26.2),
 //    128-deep stages (three) above it (16384^3 5141 us against 5359; equal
@@ -296,6 +298,7 @@ constexpr int64_t kOneWave = 152;
 constexpr int64_t kSmallK = 512;
 constexpr int64_t kOnePairWave = 76;
 constexpr int64_t kShortK = 256;
+constexpr int64_t kPairMinK = 2048;
 constexpr int64_t kDeepK = 4096;
 // Stream-K pays only where its partial sums are small next to a tile's k
 // loop: the fp32 partial of a shared tile is written and read back through
@@ -321,8 +324,8 @@ int auto_cfg(int64_t M, int64_t N, int64_t K)
     if (narrow_tiles <= kOneWave && (M <= 128 || K <= kSmallK)) return GEMM_TILE_128x64x64;
     if (M <= 128) return GEMM_TILE_128x256x64;
     if (2 * pair_tiles <= kOnePairWave) return K > kSmallK ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x128x64;
-    if (pair_tiles < kOnePairWave || K <= kShortK) return GEMM_TILE_128x256x64;
-    if (K >= kStreamKMinK && 2 * (pair_tiles % kOnePairWave) > kOnePairWave &&
+    if ((pair_tiles < kOnePairWave && K < kPairMinK) || K <= kShortK) return GEMM_TILE_128x256x64;
+    if (K >= kStreamKMinK && pair_tiles >= kOnePairWave && 2 * (pair_tiles % kOnePairWave) > kOnePairWave &&
         pair_tiles <= kStreamKMaxWaves * kOnePairWave)
         return GEMM_TILE_256x256x64_PAIR_STREAMK;
     return K <= kDeepK ? GEMM_TILE_256x256x64_PAIR : GEMM_TILE_256x256x128_PAIR;

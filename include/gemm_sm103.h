@@ -83,9 +83,10 @@ typedef enum {
                                  M <= 128 or K <= 512; else 128x64x64 on the same terms; 128x256x64 when M <= 128; with at most
                                  38 tiles of 256x256 (every one split into column halves),
                                  256x256x128_PAIR if K > 512, else 128x128x64; 128x256x64
-                                 with fewer than 76 (less than one wave of CTA pairs) or
-                                 K <= 256; 256x256x64_PAIR_STREAMK when K >= 4096, there are
-                                 at most 8 waves of 76 and the last one holds more than 38;
+                                 with fewer than 76 (less than one wave of CTA pairs) and
+                                 K < 2048, or with K <= 256; 256x256x64_PAIR_STREAMK when
+                                 K >= 4096, there are 76 to 608 (one to eight waves) and the
+                                 last wave holds more than 38;
                                  otherwise 256x256x64_PAIR up to K = 4096 and
                                  256x256x128_PAIR above */
     GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */

@@ -47,7 +47,9 @@ def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_AUTO, M=129, N=8192, K=1024) == (256, 256, 128)   # 32 pair tiles: all split
     assert g.tile_shape(g.TILE_AUTO, M=129, N=10240, K=1024) == (128, 256, 64)   # 40 pair tiles: under one wave
     assert g.tile_shape(g.TILE_AUTO, M=2048, N=1024, K=512) == (128, 128, 64)    # 32 pair tiles, short K
-    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2048, K=2048) == (128, 256, 64)   # 64 pair tiles
+    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2048, K=2048) == (256, 256, 64)   # 64 pair tiles, K >= 2048
+    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2048, K=1024) == (128, 256, 64)   # 64 pair tiles, shorter K
+    assert g.tile_config(g.TILE_AUTO, M=2048, N=2048, K=4096) == g.TILE_256x256x64_PAIR  # under a wave: no stream-K
     assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4096) == (256, 256, 64)   # 80 pair tiles, K <= 4096
     assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4097) == (256, 256, 128)  # deeper K
     assert g.tile_shape(g.TILE_AUTO, M=4096, N=3072, K=256) == (128, 256, 64)    # few k steps
