@@ -222,7 +222,7 @@ __device__ __forceinline__ size_t sk_block(int32_t slot, uint32_t rank, int q)
     return ((static_cast<size_t>(slot) * 2 + rank) * 4 + static_cast<size_t>(q)) * (32u * TN);
 }
 
-// Stream-K tail: this warp's 32 accumulator rows, unrounded, to its workspace
+// Stream-K head: this warp's 32 accumulator rows, unrounded, to its workspace
 // block (see sk_block). release() runs once every tensor-memory read is done.
 template <int TN, class Release>
 __device__ __forceinline__ void epilogue_store_partial(uint32_t t_row, uint4* ws, int lane, Release release)

@@ -80,8 +80,9 @@ typedef enum {
                                  when there are at most 38 tiles of 128x128 and K >= 2048
                                  (K >= 1024 when M <= 128);
                                  64x64x64 when its tiles fit one wave (at most 152) and
-                                 M <= 128 or K <= 512; else 128x64x64 on the same terms; 128x256x64 when M <= 128; with at most
-                                 38 tiles of 256x256 (every one split into column halves),
+                                 M <= 128 or K <= 512; else 128x64x64 on the same terms;
+                                 128x256x64 when M <= 128; with at most 38 tiles of 256x256
+                                 (every one split into column halves),
                                  256x256x128_PAIR if K > 512, else 128x128x64; 128x256x64
                                  with fewer than 76 (less than one wave of CTA pairs) and
                                  K < 2048, or with K <= 256; 256x256x64_PAIR_STREAMK when
