@@ -139,6 +139,7 @@ struct PairUnit {
     int32_t half;    // -1: the whole 256-column tile; 0 / 1: columns [0,128) / [128,256)
     int32_t kb, ke;  // k steps [kb, ke) of the tile
     int32_t role;    // kUnitWhole, kUnitHead or kUnitTail
+    bool rev;        // k steps taken from ke - 1 down to kb (every other whole unit of a cluster)
     bool last;       // the cluster's last unit
 };
 
@@ -162,13 +163,22 @@ __device__ __forceinline__ PairUnit pair_unit(int32_t u, const GemmParams& p)
 
 // The units one cluster processes, in order; every warp walks its own copy,
 // so the producer, MMA and epilogue warps see the same sequence.
+//
+// A cluster's whole-tile units alternate their k direction: its 1st, 3rd, ...
+// unit sweeps k upwards, its 2nd, 4th, ... downwards. The clusters' j-th units
+// run side by side as one wave, and consecutive waves of the grouped order
+// share A and B panels; a wave that starts where the previous one ended finds
+// the panel chunks that wave touched last still in L2, where an upward sweep
+// after an upward sweep needs the chunks it touched first, long evicted once a
+// wave's panels outgrow the cache.
 template <bool kStreamK>
 struct UnitWalk {
     int32_t u, step;     // next whole-tile unit and the stride (the cluster count)
     int32_t it, it_end;  // stream-K: the cluster's remaining iteration range, taken from its end
+    bool flip;           // direction of the next whole unit
 
     __device__ __forceinline__ UnitWalk(int32_t pair, int32_t num_pairs, const GemmParams& p)
-        : u(pair), step(num_pairs), it(0), it_end(0)
+        : u(pair), step(num_pairs), it(0), it_end(0), flip(false)
     {
         if constexpr (kStreamK) {
             const int64_t T = p.sk_iters;
@@ -182,6 +192,8 @@ struct UnitWalk {
         if constexpr (!kStreamK) {
             if (u >= p.num_units) return false;
             r = pair_unit(u, p);
+            r.rev = flip;
+            flip = !flip;
             u += step;
             r.last = u >= p.num_units;
             return true;
@@ -192,6 +204,8 @@ struct UnitWalk {
                 r.kb = 0;
                 r.ke = KT;
                 r.role = kUnitWhole;
+                r.rev = flip;
+                flip = !flip;
                 u += step;
             } else {
                 if (it >= it_end) return false;
@@ -203,6 +217,7 @@ struct UnitWalk {
                 // ends begins at k step 0 (a head, unless the whole tile) and
                 // the piece where it starts runs to the last k step (a tail)
                 r.role = r.kb > 0 ? kUnitTail : (r.ke < KT ? kUnitHead : kUnitWhole);
+                r.rev = false;
                 it_end = t * KT + r.kb;
             }
             r.half = -1;
@@ -335,11 +350,11 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                                                      static_cast<int32_t>(rank) * (Cfg::CTA_N / 2);
                 const int nbox = un.half < 0 ? Cfg::CTA_N / 64 : Cfg::CTA_N / 128;
                 const uint32_t tx = un.half < 0 ? Cfg::PAIR_STAGE_TX : Cfg::PAIR_STAGE_TX_HALF;
-                for (int32_t kt = un.kb; kt < un.ke; ++kt) {
+                for (int32_t i = 0; i < un.ke - un.kb; ++i) {
                     ok = warp_wait_phase<true>(&empty[stage], phase ^ 1u, w, kWhereProducer);
                     if (!ok) break;
                     const uint32_t fb = full0_even + 8u * static_cast<uint32_t>(stage);
-                    const int32_t k0 = kt * Cfg::TK;
+                    const int32_t k0 = (un.rev ? un.ke - 1 - i : un.kb + i) * Cfg::TK;
                     if (elect_one()) {
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
 #pragma unroll
@@ -386,7 +401,8 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * Cfg::ACC_COLS;
-                for (int32_t kt = un.kb; kt < un.ke; ++kt) {
+                const int32_t nk = un.ke - un.kb;  // the stages arrive in the producer's k order
+                for (int32_t i = 0; i < nk; ++i) {
                     ok = warp_wait_phase(&full[stage], phase, w, kWhereMma);
                     if (!ok) break;
                     tc_fence_after_sync();
@@ -402,9 +418,9 @@ __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < Cfg::TK / 16; ++kk)
-                            tc_mma_f16_ss_pair(d_tmem, ad[kk], bd[kk], idesc, (kt > un.kb || kk > 0) ? 1u : 0u);
+                            tc_mma_f16_ss_pair(d_tmem, ad[kk], bd[kk], idesc, (i > 0 || kk > 0) ? 1u : 0u);
                         tc_commit_pair_multicast(smem_addr(&empty[stage]), 0x3);  // the stage is free in both CTAs
-                        if (kt == un.ke - 1)  // accumulator complete, in both CTAs
+                        if (i == nk - 1)  // accumulator complete, in both CTAs
                             tc_commit_pair_multicast(smem_addr(&acc_full[buf]), 0x3);
                     }
                     __syncwarp();

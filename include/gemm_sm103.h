@@ -94,7 +94,16 @@ typedef enum {
     GEMM_TILE_128x64x32 = 2,  /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
                                  BLOCK_SIZE_N 64, BLOCK_SIZE_K 32) */
     GEMM_TILE_256x256x64_PAIR = 3, /* a 2-CTA cluster per tile (tcgen05 cta_group::2): each
-                                 CTA stages 128 rows of A and 128 columns of B, 6 stages */
+                                 CTA stages 128 rows of A and 128 columns of B, 6 stages.
+                                 The pair configurations (3, 4, 8, 9) alternate the k
+                                 direction over each cluster's tiles: its 2nd, 4th, ... tile
+                                 sums its k steps from the last down to the first, so a wave
+                                 of tiles starts on the panel chunks the previous wave left
+                                 in L2. The fp32 sum order of a tile thus depends on its
+                                 place in the schedule: fixed for a given device, shape,
+                                 group_size_m and configuration (repeated calls give the same
+                                 bits); with two group sizes an entry of a tile past the
+                                 first wave may round one fp16 ulp apart */
     GEMM_TILE_256x256x128_PAIR = 4, /* as 3 with 128-deep k steps, 3 stages */
     GEMM_TILE_128x128x64 = 5, /* 1 CTA per tile, 6 stages: twice the tiles of 128x256 for
                                  problems with few tiles */

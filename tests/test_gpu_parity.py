@@ -131,7 +131,8 @@ def test_single_narrowing_on_device(gemm_lib):
 
 @pytest.mark.parametrize("cfg", ALL_CFGS)
 def test_group_size_does_not_change_values(gemm_lib, cfg):
-    # the grouped order only changes which CTA computes a tile, not how
+    # the grouped order only changes which CTA computes a tile, not how (every tile of
+    # this shape is in the first wave, where the pair kernels sum k upwards)
     A, B = inputs.gemm_inputs(700, 1000, 520, seed=21)
     a, b = A.cuda(), B.cuda()
     ref = g.gemm(a, b, group_size_m=1, tile_cfg=cfg)

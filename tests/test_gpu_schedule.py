@@ -103,6 +103,39 @@ def test_kernel_walks_grouped_order(gemm_lib, M, N, K, G, cfg):
         check_against_oracle(A, B, C)
 
 
+@pytest.mark.parametrize("cfg", [g.TILE_256x256x64_PAIR, g.TILE_256x256x128_PAIR, g.TILE_256x256x128_PAIR_ALIGNED])
+def test_pair_units_alternate_k_direction(gemm_lib, cfg):
+    # A cluster's 2nd, 4th, ... unit sums its k steps downwards. Every entry of C is
+    # 2048 + 1 (k = 0, 1) + 2^-13 (k = 128) + 2^-13 (k = 256), each term in its own k step.
+    # Upwards, 2^-13 meets 2049, half an fp32 ulp there: both additions tie and keep 2049,
+    # which narrows (a tie again) to 2048. Downwards the small terms first make 2^-12, and
+    # 2049 + 2^-12 is exact in fp32 and narrows to 2050.
+    M, N, K = 2048, 256 * 20, 384
+    A = torch.zeros((M, K), dtype=torch.float16)
+    B = torch.zeros((K, N), dtype=torch.float16)
+    A[:, 0], A[:, 1], A[:, 128], A[:, 256] = 2048.0, 1.0, 2.0 ** -13, 2.0 ** -13
+    B[[0, 1, 128, 256], :] = 1.0
+    G = 8
+    C = g.gemm(A.cuda(), B.cuda(), group_size_m=G, tile_cfg=cfg).cpu().float()
+    assert g.query_status() == g.GEMM_OK
+    plan = g.launch_plan(M, N, K, tile_cfg=cfg)
+    clusters = plan["grid_ctas"] // 2
+    tiles = plan["num_tiles"]
+    split = plan["split_tiles"]
+    full = tiles - split
+    assert tiles > clusters                # some clusters take a second unit
+    order = tm.tile_order(M, N, 256, 256, G)
+    want = torch.empty_like(C)
+    for u in range(full + 2 * split):
+        pid, half = (u, -1) if u < full else (full + (u - full) // 2, (u - full) % 2)
+        pm, pn = order[pid]
+        c0 = pn * 256 + (0 if half < 0 else 128 * half)
+        c1 = c0 + (256 if half < 0 else 128)
+        want[pm * 256:(pm + 1) * 256, c0:c1] = 2050.0 if (u // clusters) % 2 == 1 else 2048.0
+    assert torch.equal(C, want)
+    assert (want == 2050.0).any() and (want == 2048.0).any()
+
+
 def test_short_trace_is_refused_before_launch(gemm_lib):
     # the kernels write 3 entries per tile: a shorter trace would be written past its end
     A, B = inputs.gemm_inputs(512, 512, 64, seed=5)
