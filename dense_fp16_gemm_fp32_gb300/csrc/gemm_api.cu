@@ -256,15 +256,20 @@ int32_t tuned_cfg(int64_t M, int64_t N, int64_t K)
 // The untuned rule of GEMM_TILE_AUTO, from device times per call of every
 // configuration on one GB300 (CUDA graphs, back-to-back calls overlapping
 // through programmatic dependent launch; the workload shapes, square
-// 512..16384, and low-K and few-tile variants of them). Problems with few
-// tiles are bound by each CTA's operand loads (about 60 bytes per cycle into
-// one SM), so there the tile that spreads the loads over the most SMs wins:
+// 512..16384, and low-K, long-K and few-tile variants of them). Problems with
+// few tiles are bound by each CTA's operand loads (about 60 bytes per cycle
+// into one SM), so there the tile that spreads the loads over the most SMs
+// wins:
 //  * few 128 x 128 tiles (at most kSplitKMaxTiles, a quarter of the SMs) with
 //    a long K (at least kSplitKMinK, or kSplitKNarrowMinK for one 128-row
-//    band): split-K across a cluster (128x4096x4096: 10.1 us against 23.1 us
-//    for the one-CTA 128 x 256 tile; 512x512x2048 6.7 against 8.1 for the pair
-//    tile; 128x4096x1536 6.4 against 8.2 for 128 x 64 x 64; with two or more
-//    bands at K = 1024 the pair tile is 4-7 % faster);
+//    band), or at most kOneWave / 2 of them with K >= kSplitKWideMinK:
+//    split-K across a cluster (128x4096x4096: 10.1 us against 23.1 us for the
+//    one-CTA 128 x 256 tile; 512x512x2048 6.7 against 8.1 for the pair tile;
+//    128x4096x1536 6.4 against 8.2 for 128 x 64 x 64; 128x8192x8192 28.3
+//    against 35.3, 256x4096x8192 22.2 against 29.5, 1024x1024x8192 21.7
+//    against 23.0, 1024x1024x16384 39.6 against 57.3, 768x1280x4096 13.0
+//    against 13.1; with two or more bands at K = 1024 the pair tile is 4-7 %
+//    faster, and at 1024x1024x2048 8.3 against 8.6);
 //  * 64 x 64 tiles that fit one wave (kOneWave), with M <= 128 or K <=
 //    kSmallK: the one-CTA 64 x 64 x 64 tile (tcgen05 M = 64), twice the SMs
 //    of 128 x 64 (512^3 3.81 us against 4.14; 768x768x512 3.90 against 4.20;
@@ -276,30 +281,39 @@ int32_t tuned_cfg(int64_t M, int64_t N, int64_t K)
 //    3.10; 128x8192x256 3.26 against 4.57 for 128 x 256);
 //  * at most one 128-row band: the one-CTA 128 x 256 tile (half of every
 //    pair tile would be empty);
-//  * at most kOnePairWave / 2 tiles of 256 x 256, each of which the pair
-//    kernel splits into two column halves (twice the SMs): the CTA-pair
-//    128-deep tile when K > kSmallK (2048x1024x1024 6.49 us against 8.34 for
-//    128 x 256; 768^3 4.96 against 5.22 for 128 x 64 x 64), else the one-CTA
-//    128 x 128 tile (2048x1024x512 4.96 against 5.05 for the pair tile);
+//  * at most kOnePairWave / 2 tiles of 256 x 256: with K >= kSkHalvesMinK
+//    the stream-K form that splits every tile into two k halves on two
+//    clusters (1536x1536x10240 32.8 us against 36.9, 1536x1536x16384 47.3
+//    against 63.4, 2048x1024x16384 45.8 against 61.9; at K = 8192 it loses
+//    2-10 %: its partial sums cost a few microseconds); below, the CTA-pair
+//    128-deep tile, which the pair kernel splits into two column halves
+//    (twice the SMs), when K > kSmallK (2048x1024x1024 6.49 us against 8.34
+//    for 128 x 256; 768^3 4.96 against 5.22 for 128 x 64 x 64; 1536x1536x8192
+//    25.9 against 30.1 for the 64-deep one), else the one-CTA 128 x 128 tile
+//    (2048x1024x512 4.96 against 5.05 for the pair tile);
 //  * less than one wave of pair tiles with K < kPairMinK, or K <= kShortK:
 //    the one-CTA 128 x 256 tile, whose epilogue and operand loads suit few k
 //    steps (4096x3072x128 7.25 us; 2048x2048x1024 8.67 against 8.80 for the
 //    64-deep pair tile); from K = kPairMinK the pair tile is 3-6 % faster
 //    there (2048^3 13.46 against 13.84 us, 2048x2048x4096 21.98 against
 //    23.41, 2048x1536x3072 and its 48 tiles 17.48 against 18.60);
-//  * otherwise the CTA-pair tile: 64-deep stages (six) up to K = kDeepK
-//    (4096^3 75.7 us against 77.2, ragged 4095x3000x1000 25.9 against 26.2),
-//    128-deep stages (three) above it (16384^3 5141 us against 5359; equal
-//    per unit of power at 8192^3, where both run power-capped).
+//  * otherwise the CTA-pair tile with 64-deep stages (six), or its stream-K
+//    form (below); since the pair kernels alternate the k direction the
+//    64-deep stages beat the 128-deep ones at every K measured, in CUDA
+//    graphs (8192^3 556.5 us against 575.8, 6144^3 240.3 against 247.7,
+//    2048x2048x8192 39.7 against 41.8, 4096x4096x8192 147.9 against 153.8,
+//    16384^3 5075 against 5111) and power-capped over seconds (8192^3 1707.5
+//    against 1689.1 TFLOP/s, 16384^3 1722.5 against 1708.8).
 constexpr int64_t kSplitKMaxTiles = 38;
 constexpr int64_t kSplitKMinK = 2048;
 constexpr int64_t kSplitKNarrowMinK = 1024;
+constexpr int64_t kSplitKWideMinK = 4096;
 constexpr int64_t kOneWave = 152;
 constexpr int64_t kSmallK = 512;
 constexpr int64_t kOnePairWave = 76;
 constexpr int64_t kShortK = 256;
 constexpr int64_t kPairMinK = 2048;
-constexpr int64_t kDeepK = 4096;
+constexpr int64_t kSkHalvesMinK = 10240;
 // Stream-K pays only where its partial sums are small next to a tile's k
 // loop: the fp32 partial of a shared tile is written and read back through
 // the SMs' operand path, which is what bounds these kernels, so each shared
@@ -320,15 +334,19 @@ int auto_cfg(int64_t M, int64_t N, int64_t K)
     const int64_t m64_tiles = ((M + 63) / 64) * ((N + 63) / 64);
     if (small_tiles <= kSplitKMaxTiles && (K >= kSplitKMinK || (M <= 128 && K >= kSplitKNarrowMinK)))
         return GEMM_TILE_128x128x64_SPLITK;
+    if (2 * small_tiles <= kOneWave && K >= kSplitKWideMinK) return GEMM_TILE_128x128x64_SPLITK;
     if (m64_tiles <= kOneWave && (M <= 128 || K <= kSmallK)) return GEMM_TILE_64x64x64;
     if (narrow_tiles <= kOneWave && (M <= 128 || K <= kSmallK)) return GEMM_TILE_128x64x64;
     if (M <= 128) return GEMM_TILE_128x256x64;
-    if (2 * pair_tiles <= kOnePairWave) return K > kSmallK ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x128x64;
+    if (2 * pair_tiles <= kOnePairWave) {
+        if (K >= kSkHalvesMinK) return GEMM_TILE_256x256x64_PAIR_STREAMK;
+        return K > kSmallK ? GEMM_TILE_256x256x128_PAIR : GEMM_TILE_128x128x64;
+    }
     if ((pair_tiles < kOnePairWave && K < kPairMinK) || K <= kShortK) return GEMM_TILE_128x256x64;
     if (K >= kStreamKMinK && pair_tiles >= kOnePairWave && 2 * (pair_tiles % kOnePairWave) > kOnePairWave &&
         pair_tiles <= kStreamKMaxWaves * kOnePairWave)
         return GEMM_TILE_256x256x64_PAIR_STREAMK;
-    return K <= kDeepK ? GEMM_TILE_256x256x64_PAIR : GEMM_TILE_256x256x128_PAIR;
+    return GEMM_TILE_256x256x64_PAIR;
 }
 
 // GEMM_TILE_AUTO: the configuration gemm_autotune chose for this shape on
@@ -540,6 +558,7 @@ int pair_clusters(DeviceState* d, int cfg_id, int64_t* clusters)
 struct SkPlan {
     int32_t first_tile;
     int32_t iters;
+    int32_t clusters;  // clusters of the launch, each taking one contiguous range of the iterations
     float* ws;
     uint32_t* flags;
 };
@@ -613,7 +632,8 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
         p.sk_flags = sk->flags;
         p.num_full_tiles = p.num_tiles;
         p.num_units = p.num_tiles;
-        pairs = slots;  // the plan splits the iterations over exactly these clusters
+        if (sk->clusters < 1 || sk->clusters > slots) return GEMM_ERR_UNSUPPORTED;
+        pairs = sk->clusters;  // the plan splits the iterations over exactly these clusters
     } else {
         const int64_t split = split_tail_tiles(num_tiles, slots);
         p.num_full_tiles = static_cast<int32_t>(num_tiles - split);
@@ -635,20 +655,40 @@ int launch_pair(const Problem& pr, int cfg_id, int32_t* trace, cudaStream_t stre
 }
 
 // ---------------------------------------------------------------- stream-K
-// Tiles of a stream-K launch on `clusters` resident clusters, or 0 when the
-// plain pair schedule is used instead: stream-K when there is at least one
-// full wave and the last partial wave holds more than half of the clusters
-// (at most half: the split tail halves it without any partial sums). The
-// last partial wave plus one full wave are split by k iterations, so every
-// cluster's range holds at least one tile's k steps.
-int64_t streamk_tiles(int64_t tiles, int64_t k_tiles, int64_t clusters)
+// The stream-K schedule of a launch on `clusters` resident clusters: how many
+// tiles (the last ones) are split by k iterations, 0 when the plain pair
+// schedule runs instead, and how many clusters the launch uses. Two forms:
+//  * at least one full wave, and a last partial wave holding more than half
+//    of the clusters (at most half: the split tail halves it without any
+//    partial sums): that wave plus one full wave are split over every
+//    cluster, so each cluster's range holds at least one tile's k steps;
+//  * no full wave, at most half of the clusters holding a tile each, and at
+//    least kSkHalvesMinKTiles (64-deep) k steps per tile: every tile is split
+//    into two k halves on two clusters (2 x tiles clusters), full-width
+//    pieces where the split tail's column halves take in more operand bytes
+//    per flop.
+// Either way a tile is shared by at most two clusters: the lower one's piece
+// starts at k step 0, the upper one's ends at the last k step.
+constexpr int64_t kSkHalvesMinKTiles = kSkHalvesMinK / 64;
+
+struct SkShape {
+    int64_t tiles;     // split tiles, 0: no stream-K
+    int64_t clusters;  // clusters of the launch
+};
+
+SkShape streamk_shape(int64_t tiles, int64_t k_tiles, int64_t clusters)
 {
-    if (clusters <= 0 || k_tiles <= 0 || tiles < clusters) return 0;
+    const SkShape none{0, 0};
+    if (clusters <= 0 || k_tiles <= 0 || tiles <= 0) return none;
+    if (tiles < clusters) {
+        if (2 * tiles > clusters || k_tiles < kSkHalvesMinKTiles || tiles * k_tiles > INT32_MAX) return none;
+        return SkShape{tiles, 2 * tiles};
+    }
     const int64_t rem = tiles % clusters;
-    if (2 * rem <= clusters) return 0;
+    if (2 * rem <= clusters) return none;
     const int64_t sk = rem + clusters;
-    if (sk * k_tiles > INT32_MAX) return 0;
-    return sk;
+    if (sk * k_tiles > INT32_MAX) return none;
+    return SkShape{sk, clusters};
 }
 
 // Stream-K workspace of one stream on one device: partial tiles and flags for
@@ -738,16 +778,16 @@ int launch_streamk(const Problem& pr, int32_t* trace, cudaStream_t stream)
     using Cfg = CfgPair256StreamK;
     const int64_t tiles = ((pr.M + Cfg::TM - 1) / Cfg::TM) * ((pr.N + Cfg::TN - 1) / Cfg::TN);
     const int64_t k_tiles = (pr.K + Cfg::TK - 1) / Cfg::TK;
-    const int64_t sk_tiles = streamk_tiles(tiles, k_tiles, clusters);
-    if (sk_tiles > 0 && tiles <= INT32_MAX) {
+    const SkShape sk = streamk_shape(tiles, k_tiles, clusters);
+    if (sk.tiles > 0 && tiles <= INT32_MAX) {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return cuda_fail(e);
         SkSpace* sp = nullptr;
         rc = sk_space(dev, stream, 2 * clusters, &sp);
         if (rc == GEMM_OK) {
-            const SkPlan plan{static_cast<int32_t>(tiles - sk_tiles), static_cast<int32_t>(sk_tiles * k_tiles), sp->ws,
-                              sp->flags};
+            const SkPlan plan{static_cast<int32_t>(tiles - sk.tiles), static_cast<int32_t>(sk.tiles * k_tiles),
+                              static_cast<int32_t>(sk.clusters), sp->ws, sp->flags};
             return launch_pair<Cfg>(pr, GEMM_TILE_256x256x64_PAIR_STREAMK, trace, stream, &plan);
         }
         if (rc != GEMM_ERR_UNSUPPORTED) return rc;
@@ -1194,11 +1234,12 @@ int gemm_launch_plan(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t*
              : cfg == GEMM_TILE_256x256x128_PAIR_ALIGNED ? pair_clusters<CfgPair256Aligned>(d, cfg, &clusters)
                                                       : pair_clusters<CfgPair256StreamK>(d, cfg, &clusters);
         if (rc != GEMM_OK) return rc;
-        const int64_t sk = cfg == GEMM_TILE_256x256x64_PAIR_STREAMK ? streamk_tiles(tiles, (K + tk - 1) / tk, clusters)
-                                                                   : 0;
-        if (sk > 0) {  // stream-K: every resident cluster; split_tiles reports the stream-K tiles
-            split = sk;
-            ctas = 2 * clusters;
+        const SkShape sk = cfg == GEMM_TILE_256x256x64_PAIR_STREAMK
+                               ? streamk_shape(tiles, (K + tk - 1) / tk, clusters)
+                               : SkShape{0, 0};
+        if (sk.tiles > 0) {  // stream-K: split_tiles reports the stream-K tiles
+            split = sk.tiles;
+            ctas = 2 * sk.clusters;
         } else {
             split = split_tail_tiles(tiles, clusters);
             const int64_t units = tiles + split;

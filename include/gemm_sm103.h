@@ -78,18 +78,17 @@ typedef enum {
     GEMM_TILE_AUTO = 0,       /* the library picks: the configuration gemm_autotune chose for
                                  this (M, N, K) on the current device; else 128x128x64_SPLITK
                                  when there are at most 38 tiles of 128x128 and K >= 2048
-                                 (K >= 1024 when M <= 128);
+                                 (K >= 1024 when M <= 128), or at most 76 and K >= 4096;
                                  64x64x64 when its tiles fit one wave (at most 152) and
                                  M <= 128 or K <= 512; else 128x64x64 on the same terms;
-                                 128x256x64 when M <= 128; with at most 38 tiles of 256x256
-                                 (every one split into column halves),
-                                 256x256x128_PAIR if K > 512, else 128x128x64; 128x256x64
-                                 with fewer than 76 (less than one wave of CTA pairs) and
-                                 K < 2048, or with K <= 256; 256x256x64_PAIR_STREAMK when
-                                 K >= 4096, there are 76 to 608 (one to eight waves) and the
-                                 last wave holds more than 38;
-                                 otherwise 256x256x64_PAIR up to K = 4096 and
-                                 256x256x128_PAIR above */
+                                 128x256x64 when M <= 128; with at most 38 tiles of 256x256,
+                                 256x256x64_PAIR_STREAMK if K >= 10240 (every tile in two k
+                                 halves), 256x256x128_PAIR if K > 512 (every tile in two
+                                 column halves), else 128x128x64; 128x256x64 with fewer than
+                                 76 (less than one wave of CTA pairs) and K < 2048, or with
+                                 K <= 256; 256x256x64_PAIR_STREAMK when K >= 4096, there are
+                                 76 to 608 (one to eight waves) and the last wave holds more
+                                 than 38; otherwise 256x256x64_PAIR */
     GEMM_TILE_128x256x64 = 1, /* 1 CTA per tile, 4-stage TMA ring, 2 TMEM accumulators */
     GEMM_TILE_128x64x32 = 2,  /* the notebook's worked-example tile (BLOCK_SIZE_M 128,
                                  BLOCK_SIZE_N 64, BLOCK_SIZE_K 32) */
@@ -128,10 +127,13 @@ typedef enum {
                                  wave of tiles holds more than half of the resident clusters
                                  (and there is at least one full wave): that wave and one full
                                  wave are split by k iterations, one contiguous range per
-                                 cluster; a tile shared by two clusters has its first k steps'
-                                 fp32 partial sums passed through a workspace and added before
-                                 the one fp16 rounding (a fixed order: results are
-                                 deterministic). Elsewhere it runs as 3. The workspace (about
+                                 cluster; and where at most half of the resident clusters
+                                 hold a tile each with K >= 10240 (160 k steps of 64): every
+                                 tile split into two k halves on two clusters. A tile shared
+                                 by two clusters has its first k steps' fp32 partial sums
+                                 passed through a workspace and added before the one fp16
+                                 rounding (a fixed order: results are deterministic).
+                                 Elsewhere it runs as 3. The workspace (about
                                  40 MB: 2 x resident clusters x 256 KiB, plus flags) is
                                  allocated on the first stream-K launch on each stream of a
                                  device and kept until exit; make that first call outside
@@ -305,7 +307,9 @@ int gemm_tile_config(int32_t tile_cfg, int64_t M, int64_t N, int64_t K, int32_t*
  *                are whole tiles taken in turn by the clusters, and the
  *                S x ceil(K/64) iterations of the others are split into one
  *                contiguous range per cluster, cluster c holding iterations
- *                [c*I/C, (c+1)*I/C) (I iterations, C = grid_ctas / 2).
+ *                [c*I/C, (c+1)*I/C) (I iterations, C = grid_ctas / 2:
+ *                every resident cluster, or 2 S clusters for the k-halves form,
+ *                where S = num_tiles).
  * Host pointers, each may be NULL. Sets up the configuration's per-device
  * state on first use (like a launch). GEMM_ERR_CUDA without a device.
  */

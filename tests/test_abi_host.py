@@ -51,7 +51,7 @@ def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_AUTO, M=2048, N=2048, K=1024) == (128, 256, 64)   # 64 pair tiles, shorter K
     assert g.tile_config(g.TILE_AUTO, M=2048, N=2048, K=4096) == g.TILE_256x256x64_PAIR  # under a wave: no stream-K
     assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4096) == (256, 256, 64)   # 80 pair tiles, K <= 4096
-    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4097) == (256, 256, 128)  # deeper K
+    assert g.tile_shape(g.TILE_AUTO, M=2048, N=2560, K=4097) == (256, 256, 64)   # deeper K: 64-deep as well
     assert g.tile_shape(g.TILE_AUTO, M=4096, N=3072, K=256) == (128, 256, 64)    # few k steps
     assert g.tile_shape(g.TILE_AUTO, M=512, N=512, K=512) == (64, 64, 64)        # 64 tiles of 64x64, short K
     assert g.tile_shape(g.TILE_AUTO, M=1024, N=1024, K=512) == (128, 64, 64)     # 128 of them: one wave
@@ -59,15 +59,24 @@ def test_tile_shapes(lib):
     assert g.tile_shape(g.TILE_AUTO, M=1024, N=768, K=128) == (128, 64, 64)
     assert g.tile_shape(g.TILE_AUTO, M=1024, N=2048, K=256) == (128, 128, 64)    # 256 tiles of 128x64: two waves
     assert g.tile_shape(g.TILE_AUTO, M=128, N=4096, K=4096) == (128, 128, 64)    # split-K
-    assert g.tile_shape(g.TILE_AUTO, M=8192, N=8192, K=8192) == (256, 256, 128)
-    assert g.tile_shape(g.TILE_AUTO, M=16384, N=16384, K=16384) == (256, 256, 128)
+    assert g.tile_shape(g.TILE_AUTO, M=8192, N=8192, K=8192) == (256, 256, 64)
+    assert g.tile_shape(g.TILE_AUTO, M=16384, N=16384, K=16384) == (256, 256, 64)
     # stream-K: 192 pair tiles (a last wave of 40 of 76) with K >= 4096; not for shorter K or many waves
     assert g.tile_config(g.TILE_AUTO, M=4096, N=3072, K=8192) == g.TILE_256x256x64_PAIR_STREAMK
     assert g.tile_config(g.TILE_AUTO, M=4096, N=3072, K=4096) == g.TILE_256x256x64_PAIR_STREAMK
     assert g.tile_config(g.TILE_AUTO, M=4096, N=3072, K=2048) == g.TILE_256x256x64_PAIR
     assert g.tile_config(g.TILE_AUTO, M=4095, N=3000, K=1000) == g.TILE_256x256x64_PAIR
-    assert g.tile_config(g.TILE_AUTO, M=8192, N=8192, K=8192) == g.TILE_256x256x128_PAIR   # last wave of 36
-    assert g.tile_config(g.TILE_AUTO, M=16384, N=16384, K=16384) == g.TILE_256x256x128_PAIR  # 54 waves
+    assert g.tile_config(g.TILE_AUTO, M=8192, N=8192, K=8192) == g.TILE_256x256x64_PAIR    # last wave of 36
+    assert g.tile_config(g.TILE_AUTO, M=16384, N=16384, K=16384) == g.TILE_256x256x64_PAIR  # 54 waves
+    assert g.tile_config(g.TILE_AUTO, M=2048, N=2048, K=8192) == g.TILE_256x256x64_PAIR    # one wave, long K
+    # at most 76 tiles of 128 x 128 and K >= 4096: split-K over two CTAs
+    assert g.tile_config(g.TILE_AUTO, M=1024, N=1024, K=8192) == g.TILE_128x128x64_SPLITK
+    assert g.tile_config(g.TILE_AUTO, M=128, N=8192, K=8192) == g.TILE_128x128x64_SPLITK
+    assert g.tile_config(g.TILE_AUTO, M=1024, N=1024, K=2048) == g.TILE_256x256x128_PAIR
+    # at most 38 pair tiles, more than 76 of 128 x 128: k halves from K = 10240
+    assert g.tile_config(g.TILE_AUTO, M=1536, N=1536, K=10240) == g.TILE_256x256x64_PAIR_STREAMK
+    assert g.tile_config(g.TILE_AUTO, M=1536, N=1536, K=8192) == g.TILE_256x256x128_PAIR
+    assert g.tile_config(g.TILE_AUTO, M=2048, N=1024, K=16384) == g.TILE_256x256x64_PAIR_STREAMK
     assert g.tile_config(g.TILE_256x256x128_PAIR_ALIGNED, 8, 8, 8) == g.TILE_256x256x128_PAIR_ALIGNED
     assert g.tile_shape(g.TILE_256x256x64_PAIR_STREAMK) == (256, 256, 64)
     assert g.tile_shape(g.TILE_256x256x64_PAIR) == (256, 256, 64)

@@ -90,5 +90,6 @@ def test_aligned_refuses_operands_tma_cannot_describe(gemm_lib):
 
 
 def test_auto_never_picks_aligned(gemm_lib):
-    assert g.tile_shape(g.TILE_AUTO, 8192, 8192, 8192) == (256, 256, 128)
+    for shape in ((8192, 8192, 8192), (4096, 4096, 4096), (1024, 1024, 1024), (256, 256, 128)):
+        assert g.tile_config(g.TILE_AUTO, *shape) != ALIGNED
     assert g.tile_shape(ALIGNED) == (256, 256, 128)

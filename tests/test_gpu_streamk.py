@@ -3,10 +3,12 @@
 Where the last partial wave of 256 x 256 tiles holds more than half of the
 resident clusters, that wave and one full wave are split by k iterations into
 one contiguous range per cluster (the stream-K decomposition of Osama et al.,
-PPoPP 2023, in its hybrid form); a tile shared by two clusters has the fp32
-partial sums of its first k steps passed through a workspace and added before
-the single fp16 rounding. Elsewhere the configuration runs the plain pair
-schedule. Every case is checked element by element against the CPU oracle.
+PPoPP 2023, in its hybrid form); where at most half of the clusters hold a
+tile each and K is long, every tile is split into two k halves on two
+clusters. A tile shared by two clusters has the fp32 partial sums of its
+first k steps passed through a workspace and added before the single fp16
+rounding. Elsewhere the configuration runs the plain pair schedule. Every
+case is checked element by element against the CPU oracle.
 """
 
 import pytest
@@ -30,11 +32,22 @@ def plan(M, N, K):
     return clusters, p["num_tiles"], p["split_tiles"]
 
 
+def resident_clusters():
+    # the plain pair schedule of a problem with many tiles uses every resident cluster
+    return g.launch_plan(8192, 8192, 64, tile_cfg=g.TILE_256x256x64_PAIR)["grid_ctas"] // 2
+
+
+HALVES_MIN_K_STEPS = 160   # 64-deep k steps per tile from which the k-halves form applies
+
+
 def expected_stream_k(tiles, k_tiles, clusters):
-    if tiles < clusters or k_tiles == 0:
-        return 0
+    """(stream-K tiles, clusters of the launch) on `clusters` resident clusters, (0, 0): plain."""
+    if tiles == 0 or k_tiles == 0:
+        return 0, 0
+    if tiles < clusters:
+        return (tiles, 2 * tiles) if 2 * tiles <= clusters and k_tiles >= HALVES_MIN_K_STEPS else (0, 0)
     rem = tiles % clusters
-    return rem + clusters if 2 * rem > clusters else 0
+    return (rem + clusters, clusters) if 2 * rem > clusters else (0, 0)
 
 
 SHAPES = [
@@ -48,15 +61,19 @@ SHAPES = [
     (4095, 3000, 1001),   # K not a multiple of 8: the workspace route repacks, then stream-K
     (4096, 3072, 8192),   # long K: where GEMM_TILE_AUTO takes stream-K (256 sampled rows)
     (4000, 3072, 4100),   # ragged M and K, 65 k steps
+    (256, 256, 10240),    # one tile in two k halves on two clusters
+    (1000, 1100, 12200),  # 20 tiles, 191 k steps (odd, the last one partial): k halves
+    (1536, 1536, 10240),  # 36 tiles on 72 clusters (256 sampled rows)
+    (2048, 1024, 10176),  # 159 k steps: just short of the k-halves form (split tail)
 ]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_stream_k_matches_oracle(gemm_lib, M, N, K):
     clusters, tiles, split = plan(M, N, K)
-    want_sk = expected_stream_k(tiles, -(-K // 64), clusters)
+    want_sk, want_clusters = expected_stream_k(tiles, -(-K // 64), resident_clusters())
     if want_sk:
-        assert split == want_sk and clusters * 2 == g.launch_plan(M, N, K, tile_cfg=SK)["grid_ctas"]
+        assert split == want_sk and clusters == want_clusters
     A, B = inputs.gemm_inputs(M, N, K, seed=M + N + K)
     a, b = A.cuda(), B.cuda()
     C = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
@@ -87,6 +104,20 @@ def test_auto_runs_stream_k_for_long_k(gemm_lib):
     check_against_oracle(A, B, C, inputs.sample_rows(M, 19))
 
 
+def test_auto_runs_k_halves_for_few_tiles_and_long_k(gemm_lib):
+    M, N, K = 1536, 1536, 10240
+    assert g.tile_config(g.TILE_AUTO, M, N, K) == SK
+    clusters, tiles, split = plan(M, N, K)
+    if resident_clusters() >= 72:
+        assert (tiles, split, clusters) == (36, 36, 72)   # every tile in two halves
+    A, B = inputs.gemm_inputs(M, N, K, seed=7)
+    a, b = A.cuda(), B.cuda()
+    C = g.gemm(a, b)
+    assert g.query_status() == g.GEMM_OK
+    assert torch.equal(C, g.gemm(a, b, tile_cfg=SK))
+    check_against_oracle(A, B, C, inputs.sample_rows(M, 29))
+
+
 def test_stream_k_small_integers_exact(gemm_lib):
     M, N, K = 4095, 3000, 1000
     gen = torch.Generator().manual_seed(11)
@@ -99,7 +130,7 @@ def test_stream_k_small_integers_exact(gemm_lib):
     assert torch.equal(C.cpu(), (A.float() @ B.float()).half())
 
 
-@pytest.mark.parametrize("M,N,K", [(4095, 3000, 1000), (3072, 3072, 136)])
+@pytest.mark.parametrize("M,N,K", [(4095, 3000, 1000), (3072, 3072, 136), (1000, 1100, 12200)])
 def test_stream_k_trace_and_schedule(gemm_lib, M, N, K):
     clusters, tiles, split = plan(M, N, K)
     G = 4
@@ -120,7 +151,7 @@ def test_stream_k_trace_and_schedule(gemm_lib, M, N, K):
             i = (pid - first) * kt + kt - 1
             want = next(c for c in range(clusters) if c * iters // clusters <= i < (c + 1) * iters // clusters)
         assert int(tr[pid, 2]) == want, (pid, int(tr[pid, 2]), want)
-    check_against_oracle(A, B, C)
+    check_against_oracle(A, B, C, inputs.sample_rows(M, 23) if M * N * K > 1.3e10 else None)
 
 
 def test_stream_k_no_store_outside_c(gemm_lib):
