@@ -43,10 +43,15 @@
 // ring and adds it to its own sums before the one fp16 narrowing. A cluster
 // only ever waits on a lower-numbered one, which the hardware dispatched
 // before it and which raises the flag without waiting on anything. The sum
-// order is fixed by the launch: results are deterministic. This follows the stream-K decomposition (Osama, Merrill,
-// Cecka, Garland and Owens, "Stream-K: Work-centric Parallel Decomposition
-// for Dense Matrix-Matrix Multiplication on the GPU", PPoPP 2023), in its
-// hybrid form (whole tiles first, one stream-K wave and a half at the end).
+// order is fixed by the launch: results are deterministic. This follows the
+// stream-K decomposition (Osama, Merrill, Cecka, Garland and Owens,
+// "Stream-K: Work-centric Parallel Decomposition for Dense Matrix-Matrix
+// Multiplication on the GPU", PPoPP 2023), in its hybrid form (whole tiles
+// first, one stream-K wave and a half at the end). The host also launches a
+// k-halves form of it for problems with few tiles and a long K: 2 x tiles
+// clusters and every tile's iterations as the stream-K range, so that each
+// cluster's range is exactly one half of one tile (a head or a tail).
+// Successive whole tiles of a cluster alternate the k direction (UnitWalk).
 // Waits are bounded as in gemm_kernel.cuh. Before a CTA may exit, its
 // producer waits until every stage has been released (so no commit still
 // targets it) and the MMA thread waits until both epilogues have released
@@ -213,9 +218,11 @@ struct UnitWalk {
                 r.kb = max(it, t * KT) - t * KT;
                 r.ke = it_end - t * KT;
                 r.pid = p.sk_first_tile + t;
-                // a range holds at least KT iterations, so the piece where it
-                // ends begins at k step 0 (a head, unless the whole tile) and
-                // the piece where it starts runs to the last k step (a tail)
+                // a range holds at least KT iterations, or (the k-halves form)
+                // is exactly the first or the second half of one tile, so the
+                // piece where it ends begins at k step 0 (a head, unless the
+                // whole tile) and the piece where it starts runs to the last
+                // k step (a tail)
                 r.role = r.kb > 0 ? kUnitTail : (r.ke < KT ? kUnitHead : kUnitWhole);
                 r.rev = false;
                 it_end = t * KT + r.kb;
